@@ -1,0 +1,449 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: the pages' printed byte
+figures, the IEEE binary16 decoding that numpy implements, a brute-force enumeration of a
+sequence's slots, torch's float64 scaled-dot-product attention on contiguous K/V, closed-form
+special cases, invariants (block permutation, shared = private), a literal replay of the
+sink + ring buffer, and the algebra of rotations.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_147_gb300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------------------ ledger
+def test_ledger_matches_printed_figures():
+    data = json.load(open(os.path.join(GOLDEN, "kv_ledger.json"), encoding="utf-8"))
+    assert len(data["entries"]) >= 8
+    for e in data["entries"]:
+        got = oracle.kv_bytes(*e["args"])
+        assert got == e["exact_bytes"], e["what"]
+        printed = e["printed_value"]
+        decimals = len(str(printed).split(".")[1]) if "." in str(printed) else 0
+        tol = e.get("tol", 0.5 * 10 ** (-decimals) + 1e-12)
+        assert abs(got / e["printed_unit_bytes"] - printed) <= tol, e["what"]
+
+
+def test_ledger_is_linear_in_every_factor():
+    base = oracle.kv_bytes(3, 5, 7, 11, 2, 13)
+    assert base == 2 * 3 * 5 * 7 * 11 * 2 * 13
+    for i in range(6):
+        args = [3, 5, 7, 11, 2, 13]
+        args[i] *= 2
+        assert oracle.kv_bytes(*args) == 2 * base
+
+
+# ------------------------------------------------------------------------------ fp16
+def test_f16_decoder_matches_numpy_for_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.f16_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # signed zero keeps its sign
+    assert math.copysign(1.0, ours[0x8000]) == -1.0
+
+
+# ------------------------------------------------------------------------------ slots
+def _enumerated_slots(table_row, n_blocks, bs):
+    """All slots of one sequence in logical order: its blocks in table order, each block's
+    offsets 0..bs-1 (an enumeration, not the div/mod formula)."""
+    out = []
+    for j in range(n_blocks):
+        for o in range(bs):
+            out.append(int(table_row[j]) * bs + o)
+    return out
+
+
+@pytest.mark.parametrize("bs", [16, 64, 5])
+def test_slot_mapping_equals_enumeration(bs):
+    rng = np.random.default_rng(bs)
+    B, maxb = 5, 9
+    nb = B * maxb + 3
+    tables = rng.permutation(nb)[: B * maxb].reshape(B, maxb).astype(np.int32)
+    seq, pos = [], []
+    for b in range(B):
+        for p in range(maxb * bs):
+            seq.append(b)
+            pos.append(p)
+    got = oracle.slot_mapping(seq, pos, tables, bs)
+    exp = []
+    for b in range(B):
+        exp.extend(_enumerated_slots(tables[b], maxb, bs))
+    assert np.array_equal(got, np.array(exp, dtype=np.int64))
+    # a negative position is padding
+    assert oracle.slot_mapping([0], [-1], tables, bs)[0] == -1
+
+
+# ------------------------------------------------------------------------------ ring
+@pytest.mark.parametrize("S,W", [(4, 1020), (4, 20), (0, 7), (3, 1)])
+def test_ring_slot_properties(S, W):
+    cap = S + W
+    for p in range(3 * cap + 5):
+        r = oracle.ring_slot(p, S, W)
+        if p < S:
+            assert r == p                     # sinks are fixed
+        else:
+            assert S <= r < cap               # window slots
+            assert oracle.ring_slot(p + W, S, W) == r   # period W
+    # any W consecutive window positions cover the window slots exactly once
+    for start in (S, S + 1, S + W - 1, 5 * W + S + 2):
+        got = sorted(oracle.ring_slot(p, S, W) for p in range(start, start + W))
+        assert got == list(range(S, cap))
+
+
+class _LiteralRing:
+    """Replays writes into a literal ring of S + W cells, cell index by the page's
+    piecewise Slot definition, and reports what survives (independent of the oracle's
+    closed-form valid set)."""
+
+    def __init__(self, S, W):
+        self.S, self.W = S, W
+        self.cell = {}
+        self.L = 0
+
+    def slot(self, p):
+        return p if p < self.S else self.S + (p - self.S) % self.W
+
+    def append(self, n=1):
+        for _ in range(n):
+            self.cell[self.slot(self.L)] = self.L
+            self.L += 1
+
+    def rollback(self, n):
+        if self.L >= n:
+            self.L -= n
+
+    def visible(self):
+        return sorted(p for p in self.cell.values() if p < self.L)
+
+
+def _hw(ring):
+    return max(ring.cell.values()) + 1 if ring.cell else 0
+
+
+@pytest.mark.parametrize("S,W", [(4, 20), (4, 1020), (2, 5)])
+def test_ring_valid_set_matches_literal_replay(S, W):
+    rng = np.random.default_rng(S * 100 + W)
+    ring = _LiteralRing(S, W)
+    for step in range(400):
+        ring.append(int(rng.integers(1, 6)))
+        if rng.random() < 0.4:
+            n = int(rng.integers(0, 4))
+            # precondition of the valid-set rule: a rollback never reaches below hw - W
+            if ring.L - n >= _hw(ring) - W:
+                ring.rollback(n)
+        hw = _hw(ring)
+        got = oracle.ring_valid(ring.L, hw, S, W)
+        assert list(got) == ring.visible(), (step, ring.L, hw)
+        if hw == ring.L:
+            assert len(got) == min(ring.L, S + W)
+        slots = [oracle.ring_slot(int(p), S, W) for p in got]
+        assert len(set(slots)) == len(slots)
+
+
+def test_ring_valid_without_rollback_is_sinks_plus_last_window():
+    S, W = 4, 1020
+    for L in (1, 3, 4, 5, 1023, 1024, 1025, 5000):
+        got = list(oracle.ring_valid(L, L, S, W))
+        if L <= S + W:
+            assert got == list(range(L))
+        else:
+            assert got == list(range(S)) + list(range(L - W, L))
+
+
+def test_ring_causal_drafts():
+    S, W, P = 4, 20, 100
+    # 4 drafts at P..P+3 appended (hw = L = P + 4); draft i sees up to P + i
+    for i in range(4):
+        got = list(oracle.ring_valid(P + 4, P + 4, S, W, q_len=4, qi=i))
+        assert got == list(range(S)) + list(range(P + 4 - W, P + i + 1))
+
+
+# ------------------------------------------------------------------------------ RoPE
+def test_rope_identity_norm_and_relative_invariance():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal(128)
+    k = rng.standard_normal(128)
+    assert np.array_equal(oracle.rope(q, 0.0), q)
+    for a in (1.0, 17.0, 1019.0):
+        assert np.linalg.norm(oracle.rope(q, a)) == pytest.approx(np.linalg.norm(q), rel=1e-13)
+    for a, b in ((3, 10), (100, 40), (0, 1023)):
+        ref = oracle.rope(q, a) @ oracle.rope(k, b)
+        for c in (1, 57, 900):
+            assert oracle.rope(q, a + c) @ oracle.rope(k, b + c) == pytest.approx(ref, rel=1e-9, abs=1e-9)
+
+
+def test_rope_matches_complex_rotation():
+    """Rotate-half RoPE == multiplying the complex numbers x_i + i x_{i+D/2} by
+    exp(i * index * base^(-2i/D))."""
+    rng = np.random.default_rng(8)
+    D = 128
+    x = rng.standard_normal(D)
+    for idx in (1.0, 5.0, 1000.0):
+        z = x[: D // 2] + 1j * x[D // 2:]
+        theta = 10000.0 ** (-2.0 * np.arange(D // 2) / D)
+        z = z * np.exp(1j * idx * theta)
+        ref = np.concatenate([z.real, z.imag])
+        assert np.allclose(oracle.rope(x, idx), ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------------------ attention
+def _gather_contiguous(w, k_pool, v_pool, b, ctx):
+    """Contiguous K/V [ctx, Hkv, D] of sequence b via the slot enumeration."""
+    slots = _enumerated_slots(w.block_tables[b], (ctx + w.block_size - 1) // w.block_size,
+                              w.block_size)[:ctx]
+    blk = np.array(slots) // w.block_size
+    off = np.array(slots) % w.block_size
+    K = k_pool[blk, :, off, :].astype(np.float64)
+    V = v_pool[blk, :, off, :].astype(np.float64)
+    return K, V
+
+
+def _sdpa_reference(w, q, k_pool, v_pool, context_lens):
+    """torch float64 scaled_dot_product_attention over contiguous, enumerated K/V."""
+    B, q_len, Hq, D = q.shape
+    G = Hq // w.num_kv_heads
+    out = np.zeros((B, q_len, Hq, D))
+    for b in range(B):
+        ctx = int(context_lens[b])
+        K, V = _gather_contiguous(w, k_pool, v_pool, b, ctx)
+        Kt = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(G, dim=0)   # [Hq, ctx, D]
+        Vt = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        Qt = torch.from_numpy(q[b].astype(np.float64)).permute(1, 0, 2)        # [Hq, q_len, D]
+        mask = torch.ones(q_len, ctx, dtype=torch.bool)
+        for i in range(q_len):
+            mask[i, ctx - q_len + i + 1:] = False
+        o = torch.nn.functional.scaled_dot_product_attention(
+            Qt, Kt, Vt, attn_mask=mask, scale=w.scale)
+        out[b] = o.permute(1, 0, 2).numpy()
+    return out
+
+
+def _tiny_inputs(poison=True):
+    w = workloads.tiny()
+    k, v = w.pools(poison=poison)
+    k, v = k[0].numpy(), v[0].numpy()
+    q = w.query(0).numpy()
+    return w, q, k, v
+
+
+def _fill_appended(w, k, v):
+    """Replace the NaN-poisoned slots that the step appends with data (via the oracle)."""
+    seq, pos = w.new_token_positions()
+    slots = oracle.slot_mapping(seq, pos, w.block_tables, w.block_size)
+    kn, vn = w.new_kv(0)
+    oracle.kv_append(kn.numpy(), vn.numpy(), slots, k, v, w.block_size)
+    return slots
+
+
+def test_paged_attention_matches_torch_sdpa_tiny():
+    w, q, k, v = _tiny_inputs()
+    _fill_appended(w, k, v)
+    got = oracle.paged_attention(q, k, v, w.block_tables, w.context_lens, w.block_size, w.scale)
+    ref = _sdpa_reference(w, q, k, v, w.context_lens)
+    assert np.isfinite(got).all()
+    assert np.max(np.abs(got - ref)) < 1e-12
+
+
+def test_paged_attention_causal_multi_query_matches_sdpa():
+    rng = np.random.default_rng(11)
+    w = workloads.tiny()
+    k = rng.standard_normal((64, 2, 16, 128)).astype(np.float16)
+    v = rng.standard_normal((64, 2, 16, 128)).astype(np.float16)
+    q = rng.standard_normal((2, 4, 12, 128)).astype(np.float16)
+    got = oracle.paged_attention(q, k, v, w.block_tables, w.context_lens, 16, w.scale)
+    ref = _sdpa_reference(w, q, k, v, w.context_lens)
+    assert np.max(np.abs(got - ref)) < 1e-12
+
+
+def test_single_token_context_returns_v():
+    w, q, k, v = _tiny_inputs(poison=False)
+    lens = np.array([1, 1], dtype=np.int32)
+    got = oracle.paged_attention(q, k, v, w.block_tables, lens, 16, w.scale)
+    for b in range(2):
+        blk = w.block_tables[b, 0]
+        for h in range(12):
+            assert np.array_equal(got[b, 0, h], v[blk, h // 6, 0].astype(np.float64))
+
+
+def test_constant_keys_or_zero_query_give_mean_v():
+    w, q, k, v = _tiny_inputs(poison=False)
+    k_const = np.ones_like(k)
+    got = oracle.paged_attention(q, k_const, v, w.block_tables, w.context_lens, 16, w.scale)
+    got0 = oracle.paged_attention(np.zeros_like(q), k, v, w.block_tables, w.context_lens, 16,
+                                  w.scale)
+    for b in range(2):
+        _, V = _gather_contiguous(w, k, v, b, int(w.context_lens[b]))
+        mean = V.mean(axis=0)                                    # [Hkv, D]
+        for h in range(12):
+            assert np.allclose(got[b, 0, h], mean[h // 6], rtol=0, atol=1e-12)
+            assert np.allclose(got0[b, 0, h], mean[h // 6], rtol=0, atol=1e-12)
+
+
+def test_huge_scale_selects_argmax_value():
+    w, q, k, v = _tiny_inputs(poison=False)
+    got = oracle.paged_attention(q, k, v, w.block_tables, w.context_lens, 16, 1e6)
+    for b in range(2):
+        K, V = _gather_contiguous(w, k, v, b, int(w.context_lens[b]))
+        for h in range(12):
+            s = K[:, h // 6, :] @ q[b, 0, h].astype(np.float64)
+            assert np.array_equal(got[b, 0, h], V[int(np.argmax(s)), h // 6])
+
+
+def test_block_permutation_invariance_is_exact():
+    w, q, k, v = _tiny_inputs()
+    _fill_appended(w, k, v)
+    base = oracle.paged_attention(q, k, v, w.block_tables, w.context_lens, 16, w.scale)
+    perm = np.random.default_rng(5).permutation(64)
+    inv = np.argsort(perm)
+    k2, v2 = k[inv], v[inv]          # block j moves to position perm[j]
+    tables = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1)
+    got = oracle.paged_attention(q, k2, v2, tables, w.context_lens, 16, w.scale)
+    assert np.array_equal(got, base)
+
+
+def test_shared_prefix_equals_private_copies():
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal((20, 2, 16, 128)).astype(np.float16)
+    v = rng.standard_normal((20, 2, 16, 128)).astype(np.float16)
+    q = rng.standard_normal((3, 1, 12, 128)).astype(np.float16)
+    shared = np.array([[0, 1, 2, 3], [0, 1, 4, 5], [0, 1, 6, 7]], dtype=np.int32)
+    # private copies of blocks 0, 1 for sequences 1 and 2
+    k[8:10], v[8:10] = k[0:2], v[0:2]
+    k[10:12], v[10:12] = k[0:2], v[0:2]
+    private = np.array([[0, 1, 2, 3], [8, 9, 4, 5], [10, 11, 6, 7]], dtype=np.int32)
+    lens = np.array([60, 50, 64], dtype=np.int32)
+    a = oracle.paged_attention(q, k, v, shared, lens, 16, 0.1)
+    b = oracle.paged_attention(q, k, v, private, lens, 16, 0.1)
+    assert np.array_equal(a, b)
+
+
+def test_seq_mask_and_threads_do_not_change_results():
+    w, q, k, v = _tiny_inputs()
+    _fill_appended(w, k, v)
+    a, nt = oracle.paged_attention(q, k, v, w.block_tables, w.context_lens, 16, w.scale,
+                                   num_threads=1, return_threads=True)
+    assert nt == 1
+    b = oracle.paged_attention(q, k, v, w.block_tables, w.context_lens, 16, w.scale,
+                               num_threads=3)
+    assert np.array_equal(a, b)
+    m = oracle.paged_attention(q, k, v, w.block_tables, w.context_lens, 16, w.scale,
+                               seq_mask=np.array([0, 1]))
+    assert np.array_equal(m[1], a[1]) and not m[0].any()
+
+
+# ------------------------------------------------------------------------------ append / copy
+def test_kv_append_round_trip_and_untouched_bytes():
+    w, q, k, v = _tiny_inputs()
+    k0, v0 = k.copy(), v.copy()
+    seq, pos = w.new_token_positions()
+    slots = oracle.slot_mapping(seq, pos, w.block_tables, w.block_size)
+    kn, vn = (t.numpy() for t in w.new_kv(0))
+    slots_pad = np.concatenate([slots, [-1]])
+    kn_pad = np.concatenate([kn, np.full_like(kn[:1], 7.0)])
+    vn_pad = np.concatenate([vn, np.full_like(vn[:1], 7.0)])
+    oracle.kv_append(kn_pad, vn_pad, slots_pad, k, v, w.block_size)
+    touched = np.zeros(k.shape[0] * k.shape[2], dtype=bool)
+    for t, s in enumerate(slots):
+        blk, off = divmod(int(s), w.block_size)
+        assert k[blk, :, off].tobytes() == kn[t].tobytes()
+        assert v[blk, :, off].tobytes() == vn[t].tobytes()
+        touched[blk * w.block_size + off] = True
+    kt = k.transpose(0, 2, 1, 3).reshape(-1, 2 * 128)
+    k0t = k0.transpose(0, 2, 1, 3).reshape(-1, 2 * 128)
+    assert kt[~touched].tobytes() == k0t[~touched].tobytes()
+    assert not np.any(k == 7.0)      # the padded row went nowhere
+
+
+def test_copy_blocks_all_layers():
+    rng = np.random.default_rng(9)
+    L, NB = 3, 10
+    k = rng.standard_normal((L, NB, 2, 16, 128)).astype(np.float16)
+    v = rng.standard_normal((L, NB, 2, 16, 128)).astype(np.float16)
+    k0, v0 = k.copy(), v.copy()
+    src, dst = [1, 1, 4], [7, 8, 9]
+    oracle.copy_blocks(k, v, src, dst, L, NB * 2 * 16 * 128, 2 * 16 * 128)
+    for l in range(L):
+        for s, d in zip(src, dst):
+            assert k[l, d].tobytes() == k0[l, s].tobytes()
+            assert v[l, d].tobytes() == v0[l, s].tobytes()
+        for j in range(NB):
+            if j not in dst:
+                assert k[l, j].tobytes() == k0[l, j].tobytes()
+
+
+# ------------------------------------------------------------------------------ ring attention
+def _ring_reference(q, k, v, table, L, hw, S, W, scale, bs=16):
+    """Literal ring replay + complex-number RoPE + torch SDPA, one sequence, one kv head group."""
+    q_len, Hq, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    ring = _LiteralRing(S, W)
+    for p in range(hw):                 # positions 0..hw-1 written in order: each cell keeps
+        ring.cell[ring.slot(p)] = p     # the last position written into it
+    lo = max(S, hw - W)
+    out = np.zeros((q_len, Hq, D))
+    theta = 10000.0 ** (-2.0 * np.arange(D // 2) / D)
+
+    def rot(x, idx):
+        z = (x[..., : D // 2] + 1j * x[..., D // 2:]) * np.exp(1j * idx * theta)
+        return np.concatenate([z.real, z.imag], axis=-1)
+
+    def cidx(p):
+        return p if p < S else S + (p - lo)
+
+    for i in range(q_len):
+        vis = L - q_len + i + 1
+        pos = sorted(p for p in ring.cell.values() if p < vis)
+        rows = [ring.slot(p) for p in pos]
+        blk = np.array([table[r // bs] for r in rows])
+        off = np.array([r % bs for r in rows])
+        K = k[blk, :, off, :].astype(np.float64)
+        V = v[blk, :, off, :].astype(np.float64)
+        K = np.stack([rot(K[t], cidx(p)) for t, p in enumerate(pos)])
+        qv = rot(q[i].astype(np.float64), cidx(L - q_len + i))
+        Kt = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(G, 0)
+        Vt = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(G, 0)
+        Qt = torch.from_numpy(qv)[:, None, :]
+        out[i] = torch.nn.functional.scaled_dot_product_attention(Qt, Kt, Vt, scale=scale)[:, 0].numpy()
+    return out
+
+
+@pytest.mark.parametrize("S,W,L,hw,q_len", [(4, 1020, 5000, 5004, 4), (4, 1020, 5002, 5004, 1),
+                                             (4, 1020, 700, 700, 1), (4, 60, 130, 133, 2)])
+def test_ring_attention_matches_literal_replay(S, W, L, hw, q_len):
+    rng = np.random.default_rng(L + hw)
+    bs = 16
+    nblk = (S + W + bs - 1) // bs
+    NB = nblk + 5
+    k = rng.standard_normal((NB, 2, bs, 128)).astype(np.float16)
+    v = rng.standard_normal((NB, 2, bs, 128)).astype(np.float16)
+    table = rng.permutation(NB)[:nblk].astype(np.int32)
+    q = rng.standard_normal((1, q_len, 12, 128)).astype(np.float16)
+    got = oracle.ring_attention(q, k, v, table[None], [L], [hw], bs, S, W, 1 / math.sqrt(128))
+    ref = _ring_reference(q[0], k, v, table, L, hw, S, W, 1 / math.sqrt(128), bs)
+    assert np.max(np.abs(got[0] - ref)) < 1e-11
+
+
+def test_ring_without_rope_and_wrap_is_paged_attention():
+    """Before the ring wraps and with rotation off, ring attention is plain paged attention."""
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((70, 2, 16, 128)).astype(np.float16)
+    v = rng.standard_normal((70, 2, 16, 128)).astype(np.float16)
+    q = rng.standard_normal((2, 3, 12, 128)).astype(np.float16)
+    tables = rng.permutation(70)[:64].reshape(2, 32).astype(np.int32)
+    L = np.array([300, 511])
+    a = oracle.ring_attention(q, k, v, tables, L, L, 16, 4, 508, 0.09, rope_mode=oracle.ROPE_NONE)
+    b = oracle.paged_attention(q, k, v, tables, L.astype(np.int32), 16, 0.09)
+    assert np.max(np.abs(a - b)) < 1e-13
