@@ -1,0 +1,185 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache decode-attention library (GB300, sm_103a).
+ *
+ * The operations are the hot path of a paged KV cache:
+ *   - slot mapping: a token's logical position -> its slot in the physical block pool, through
+ *     the sequence's block table (and the sink + ring variant of that mapping);
+ *   - KV append: scatter each new token's K/V rows into its slot;
+ *   - copy-on-write block copy;
+ *   - paged decode attention: each sequence's few newest query tokens attend over all of its
+ *     cached K/V, read indirectly through its block table, with GQA head groups;
+ *   - sink + ring decode attention with RoPE applied at read time.
+ *
+ * Sources (page title, section):
+ *   [EDGE]   "端侧 SLM 显存保活术：在 4GB 内存板卡上实现轻量 PagedAttention 与 KV 缓存分块"
+ *   [OLLAMA] "Ollama的内存管理策略：从KV Cache Block分配到Prefix-aware内存复用的演进"
+ *   [RING]   streaming-inference page (wzjinhao.cn/news/69573), sections
+ *            "环形上下文与注意力沉淀机制" and "C 环形 KV 缓存管理内核实现"
+ *   [VLLM]   "大模型推理内存优化：从 KV Cache 分页到连续批处理的工程实践"
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked (device) are CUDA device pointers; (host) are host pointers. The caller
+ *     owns every buffer. Nothing here allocates device memory or synchronises the stream,
+ *     except pkv_device_error(), which reads a status word back.
+ *   - fp16 tensors are IEEE binary16 ("half"), passed as void*.
+ *   - One layer's KV pool: k_cache and v_cache, each [num_blocks][num_kv_heads][block_size]
+ *     [head_dim] contiguous, 16-byte aligned. Several layers are addressed by the caller
+ *     passing each layer's base pointer.
+ *   - head_dim must be 128. block_size must be one of 16, 32, 64, 128, 256.
+ *   - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *   - Block tables: int32 [num_seqs][max_blocks_per_seq]; entry j of row b is the physical
+ *     block holding logical block j of sequence b ([EDGE] §注意力寻址非连续物理块的间接寻址内核;
+ *     [VLLM] block-table list). Entries past a sequence's last block are never read.
+ *   - Return value: PKV_OK (0) or a negative status. Argument errors are detected on the host
+ *     before any launch. Data-dependent errors found on the device (an out-of-range block id
+ *     or context length) never fault: the kernel skips the bad access and sets a bit in the
+ *     device error word (see pkv_device_error).
+ *   - stream: a cudaStream_t (NULL = the legacy default stream).
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* pkv_stream_t;
+
+/* ---- status codes ------------------------------------------------------------------------ */
+#define PKV_OK 0
+#define PKV_EINVAL (-22)      /* bad shape, size, alignment or pointer */
+#define PKV_ERANGE (-34)      /* a host-checked index is out of range (pkv_check_*) */
+#define PKV_ENOSPC (-28)      /* workspace smaller than pkv_decode_workspace_bytes() */
+#define PKV_ECUDA_BASE (-1000) /* PKV_ECUDA_BASE - cudaError_t of a failed CUDA call */
+
+/* ---- device error word bits ---------------------------------------------------------------- */
+#define PKV_DEVERR_BLOCK_ID 1u   /* a block-table entry outside [0, num_blocks) was read */
+#define PKV_DEVERR_CONTEXT 2u    /* a context length outside [0, max_blocks*block_size] */
+#define PKV_DEVERR_SLOT 4u       /* a slot outside [-inf, num_blocks*block_size) (negative = skip) */
+#define PKV_DEVERR_TIMEOUT 8u    /* an in-kernel pipeline wait ran past its iteration limit */
+#define PKV_DEVERR_SEQ 16u       /* a sequence id outside [0, num_seqs) */
+#define PKV_DEVERR_POSITION 32u  /* a position past the sequence's block table */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int pkv_version(void);
+
+/* Reads the calling device's error word into *err_out (host) after synchronising `stream`;
+ * clears it when `clear` is non-zero. Bits: PKV_DEVERR_*. */
+int pkv_device_error(unsigned int* err_out, int clear, pkv_stream_t stream);
+
+/* ---- slot mapping ------------------------------------------------------------------------
+ * slot_out[i] = block_tables[seq_ids[i]][positions[i] / block_size] * block_size
+ *               + positions[i] % block_size,
+ * the addressing of [EDGE] §注意力寻址非连续物理块的间接寻址内核 (logical block = T / block size,
+ * offset = T % block size, physical block from the table). positions[i] < 0 gives -1
+ * (padding). A seq id or position outside the table gives -1 and sets PKV_DEVERR_SEQ /
+ * PKV_DEVERR_POSITION. All arrays (device): seq_ids int32 [n], positions int64 [n],
+ * slot_out int64 [n]. */
+int pkv_slot_mapping(const int32_t* seq_ids, const int64_t* positions, int n,
+                     const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                     int block_size, int64_t* slot_out, pkv_stream_t stream);
+
+/* Sink + ring slot mapping ([RING] §环形上下文与注意力沉淀机制): ring slot
+ *   r = positions[i]               if positions[i] < sink
+ *     = sink + (positions[i] - sink) mod window   otherwise,
+ * then slot = block_tables[seq][r / block_size] * block_size + r % block_size. The ring's
+ * sink + window slots occupy the first ceil((sink+window)/block_size) table entries.
+ * Arrays as for pkv_slot_mapping. window >= 1, sink >= 0. */
+int pkv_ring_slot_mapping(const int32_t* seq_ids, const int64_t* positions, int n,
+                          const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                          int sink, int window, int block_size, int64_t* slot_out,
+                          pkv_stream_t stream);
+
+/* ---- KV append ---------------------------------------------------------------------------
+ * For every token t with slot_mapping[t] >= 0 and every kv head h:
+ *   k_cache[slot / bs][h][slot % bs][:] = k[t][h][:]   (and the same for v),
+ * a byte copy ([VLLM] on-demand paging: a new token's K/V go into its block; [RING] AppendKV).
+ * Negative slots are skipped. A slot >= num_blocks*block_size is skipped and sets
+ * PKV_DEVERR_SLOT. k, v (device): fp16 [num_tokens][num_kv_heads][head_dim];
+ * slot_mapping (device): int64 [num_tokens]. Duplicate slots in one call race. */
+int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                  void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
+                  int block_size, pkv_stream_t stream);
+
+/* ---- copy-on-write block copy --------------------------------------------------------------
+ * For every layer l < num_layers and i < n: block dst[i] := block src[i], K and V, where
+ * layer l's pool starts layer_stride_elems fp16 elements after layer l-1's and a block is
+ * num_kv_heads*block_size*head_dim elements ([OLLAMA] §三, copy-on-write of a shared block
+ * before a write). src, dst (device): int32 [n]; ids outside [0, num_blocks) are skipped and
+ * set PKV_DEVERR_BLOCK_ID. The dst set must not overlap the src set. */
+int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n,
+                    int64_t layer_stride_elems, int num_layers, int num_blocks,
+                    int num_kv_heads, int head_dim, int block_size, pkv_stream_t stream);
+
+/* ---- decode attention ------------------------------------------------------------------------
+ * Workspace: caller-owned device scratch for split-context partial results and the per
+ * (sequence, kv head) arrival counters. Size it with pkv_decode_workspace_bytes() (for the
+ * current device; the size depends on its SM count) and zero it once with
+ * pkv_workspace_init() before first use; every decode call leaves the counters zeroed again.
+ * One workspace must not be used by two calls that run concurrently. After a call that set
+ * PKV_DEVERR_TIMEOUT, re-initialise it. */
+size_t pkv_decode_workspace_bytes(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                  int head_dim);
+int pkv_workspace_init(void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Paged decode attention ([VLLM] PagedAttention kernel paragraph: K/V read indirectly through
+ * the block table; [EDGE] addressing section). For sequence b, query token i < q_len, query
+ * head h (kv head kh = h / G):
+ *   visible tokens  t < context_lens[b] - q_len + i + 1   (causal when q_len > 1)
+ *   K_t = k_cache[block_tables[b][t / bs]][kh][t % bs][:]  (V likewise)
+ *   out[b][i][h][:] = softmax_t(scale * <q[b][i][h], K_t>) . V
+ * context_lens (device, int32 [num_seqs]) count the tokens in cache including this step's
+ * appended ones. q, out (device): fp16 [num_seqs][q_len][num_q_heads][head_dim]. fp32
+ * accumulation; the result is bit-identical for identical inputs and does not depend on which
+ * physical blocks hold the data. A sequence with no visible tokens gets zeros. Requires
+ * num_q_heads % num_kv_heads == 0 and (num_q_heads / num_kv_heads) * q_len <= 32. */
+int pkv_paged_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          int num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int num_seqs, int q_len, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size, float scale,
+                          void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* RoPE table for ring attention, written to HOST memory: cos_sin[j][i][0] = cos(j * theta_i),
+ * cos_sin[j][i][1] = sin(j * theta_i), theta_i = base^(-2i/head_dim), j < n_index,
+ * i < head_dim/2; angles computed in double, stored as float. Copy it to the device for
+ * pkv_ring_attn_decode. */
+int pkv_rope_table(float* cos_sin, int n_index, int head_dim, double base);
+
+/* Sink + ring decode attention ([RING] §环形上下文与注意力沉淀机制, §C 环形 KV 缓存管理内核实现).
+ * Sequence b's logical positions live at ring slots Slot(p) (see pkv_ring_slot_mapping) in
+ * its first ceil((sink+window)/bs) blocks. logical_len[b] = L (tokens after this step's
+ * appends), high_water[b] = hw (one past the largest position ever written), with
+ * hw - window <= L <= hw. Query i (position L - q_len + i) sees the sinks [0, min(sink, vis))
+ * and the window positions [max(sink, hw - window), vis), vis = L - q_len + i + 1.
+ * Keys are stored before RoPE and rotated at read time (rotate-half pairs (d, d + 64)) by
+ * their cache index: a sink's index is its position, a window position p has index
+ * sink + p - max(sink, hw - window); the query uses its own position's index.
+ * rope_cos_sin (device): float [sink + window][head_dim/2][2] from pkv_rope_table().
+ * logical_len, high_water (device): int64 [num_seqs]. Other arguments as for
+ * pkv_paged_attn_decode (the same workspace sizing applies). */
+int pkv_ring_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         int num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
+                         const int64_t* logical_len, const int64_t* high_water, int num_seqs,
+                         int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int sink, int window, const float* rope_cos_sin,
+                         float scale, void* workspace, size_t workspace_bytes,
+                         pkv_stream_t stream);
+
+/* ---- host-side validation (debug mode; all arrays are HOST copies) ---------------------------
+ * pkv_check_tables: every block-table entry a sequence uses (the first
+ * ceil(context_lens[b]/block_size)) is in [0, num_blocks), and 0 <= context_lens[b] <=
+ * max_blocks_per_seq*block_size. Returns PKV_OK or PKV_ERANGE; *bad_seq (if non-NULL) gets
+ * the first offending sequence.
+ * pkv_check_slots: every slot is < num_blocks*block_size and no non-negative slot repeats. */
+int pkv_check_tables(const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                     int max_blocks_per_seq, int block_size, int num_blocks, int* bad_seq);
+int pkv_check_slots(const int64_t* slots, int n, int num_blocks, int block_size, int* bad_index);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,853 @@
+// pkv_decode.cu -- paged decode attention and its sink + ring variant for sm_103a.
+//
+// What it computes ([VLLM] PagedAttention kernel paragraph; [EDGE] addressing section): each
+// sequence's q_len newest query tokens, for each query head, attend over the sequence's cached
+// K/V, which live in fixed-size physical blocks reached through the sequence's block table.
+// The ring variant ([RING] §环形上下文与注意力沉淀机制) reads the sink + ring slots and rotates
+// keys (RoPE) by their cache index at read time.
+//
+// Design (GB300):
+//  * Work unit = (sequence b, kv head h). Every query head of the GQA group of h and every
+//    query token of b forms one row of a 16-row tile (R = G * q_len rows, padded to 16 or 32),
+//    so each K/V byte is read from HBM once for the whole group.
+//  * The unit's context is cut into 16-token chunks (one chunk = 4 KB of K + 4 KB of V; a
+//    block of bs tokens is bs/16 consecutive chunks). All units' chunks form one stream, and
+//    every CTA of a persistent grid (SM count x resident CTAs) takes an equal contiguous
+//    slice of it: no CTA waits on a long sequence while others idle. A unit cut by slice
+//    boundaries leaves normalised partials (m, l, o) in the workspace; the CTA that arrives
+//    last on the unit's counter merges them in slice order (no spinning; the merge order and
+//    hence the result are independent of scheduling and of which physical blocks are used).
+//  * One producer warp walks the slice, stages the block-table entries in registers (one
+//    coalesced 32-entry load per 32 chunks: the block table never sits in the consumers'
+//    path) and issues TMA tile loads (128-byte swizzle) of K and V into an NST-deep ring of
+//    shared-memory stages, completing on mbarriers. The next chunks are in flight while the
+//    consumers work on the current one.
+//  * NCW consumer warps take the slice's chunks round-robin, each with its own online-softmax
+//    state: S = Q K^T with mma.sync m16n8k16 (f16 in, f32 accumulate; K fragments by ldmatrix
+//    from the swizzled tile), softmax in the exp2 domain, O += P V with V fragments by
+//    ldmatrix.trans. At each unit boundary the warps merge through shared memory.
+//  * No wait is unbounded: an mbarrier wait gives up after kWaitLimit polls, sets
+//    PKV_DEVERR_TIMEOUT and lets the kernel finish. Out-of-range block ids become
+//    out-of-bounds TMA boxes (zero fill) and set PKV_DEVERR_BLOCK_ID.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kD = 128;                       // head_dim
+constexpr int kChunk = 16;                    // tokens per pipeline stage
+constexpr int kHalfBytes = kChunk * 128;      // 16 rows x 64 dims x 2 B (one swizzled tile)
+constexpr int kStageBytes = 4 * kHalfBytes;   // K lo/hi + V lo/hi = 8 KB
+constexpr int kMaxCtasPerSm = 4;              // bounds the grid, hence the workspace
+constexpr int kMaxSeqs = 4096;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+struct DecodeArgs {
+  __half* out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;  // paged
+  const int64_t* logical_len;   // ring: L
+  const int64_t* high_water;    // ring: hw
+  const float* rope;            // ring: [sink + window][64][2] (cos, sin)
+  float* part_o;                // [2 * grid][R][128]
+  float* part_ml;               // [2 * grid][R][2]
+  int* counters;                // [num_seqs * Hkv]
+  unsigned int* err;
+  int num_blocks, max_blocks, num_seqs, q_len, Hq, Hkv, G, R;
+  int block_size, bs_shift;     // bs_shift = log2(block_size / 16)
+  int sink, window;
+  float scale_log2;             // scale * log2(e)
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+template <int NCW, int NST, int MT>
+struct Smem {
+  static constexpr int kQHalf = MT * 2048;            // 16*MT rows x 128 B
+  static constexpr int kQBuf = 2 * kQHalf;
+  static constexpr int kQ = NST * kStageBytes;
+  static constexpr int kBars = kQ + 2 * kQBuf;        // full[NST], empty[NST], qfull[2], qempty[2]
+  static constexpr int kFlags = kBars + (2 * NST + 4) * 8;  // abort, bcast
+  static constexpr int kScratch = kFlags + 16;
+  __host__ __device__ static int scratch_floats(int R) {  // sO + sM + sL + sW + sRow
+    return NCW * R * kD + 3 * NCW * R + 2 * R;
+  }
+  __host__ __device__ static int seq_off(int R) { return kScratch + scratch_floats(R) * 4; }
+  // per sequence: prefix (B+1 ints), length, high water
+  __host__ static size_t bytes(int R, int B) {
+    return 1024 + static_cast<size_t>(seq_off(R)) + static_cast<size_t>(3 * B + 1) * 4;
+  }
+};
+
+struct Seg {
+  int b, h, c0, c1, nb;  // chunks [c0, c1) of unit (b, h), which has nb chunks
+  int x;                 // global stream index of chunk c0
+};
+
+struct Cursor {
+  const int* pre;  // pre[b] = chunks (per kv head) of sequences < b
+  int B, Hkv, end;
+
+  __device__ __forceinline__ bool first(int a, Seg& s) const {
+    if (a >= end) return false;
+    int lo = 0, hi = B - 1;  // largest b with pre[b] * Hkv <= a
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] * Hkv <= a) lo = mid; else hi = mid - 1;
+    }
+    s.b = lo;
+    s.nb = pre[lo + 1] - pre[lo];
+    const int off = a - pre[lo] * Hkv;
+    s.h = off / s.nb;
+    s.c0 = off - s.h * s.nb;
+    s.c1 = min(s.nb, s.c0 + (end - a));
+    s.x = a;
+    return true;
+  }
+  __device__ __forceinline__ bool next(Seg& s) const {
+    const int x = s.x + (s.c1 - s.c0);
+    if (x >= end) return false;
+    // the previous segment ended its unit (it stopped short of `end`)
+    if (++s.h == Hkv) {
+      s.h = 0;
+      do { ++s.b; } while (pre[s.b + 1] == pre[s.b]);
+    }
+    s.nb = pre[s.b + 1] - pre[s.b];
+    s.c0 = 0;
+    s.c1 = min(s.nb, end - x);
+    s.x = x;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void flag_timeout(const DecodeArgs& a, volatile int* abort) {
+  atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+  *abort = 1;
+}
+
+// ---------------------------------------------------------------------------------------------
+template <int NCW, int NST, int MT, bool RING>
+__global__ void __launch_bounds__((NCW + 1) * 32, MT == 1 ? 2 : 1)
+decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
+  using L = Smem<NCW, NST, MT>;
+  constexpr int kNC = NCW * 32;  // consumer threads
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + L::kBars;
+  const uint32_t bar_empty = bar_full + NST * 8;
+  const uint32_t bar_qfull = bar_empty + NST * 8;
+  const uint32_t bar_qempty = bar_qfull + 2 * 8;
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kFlags);
+  volatile int* bcast = abort + 1;
+  float* sO = reinterpret_cast<float*>(smem + L::kScratch);
+  float* sM = sO + NCW * a.R * kD;
+  float* sL = sM + NCW * a.R;
+  float* sW = sL + NCW * a.R;
+  float* sRow = sW + NCW * a.R;
+  int* pre = reinterpret_cast<int*>(smem + L::seq_off(a.R));
+  int* slen = pre + a.num_seqs + 1;   // ctx (paged) or L (ring), clamped
+  int* shw = slen + a.num_seqs;       // ring: high water
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int B = a.num_seqs;
+  const int cap = a.sink + a.window;
+
+  // ---- per-sequence lengths and chunk counts -------------------------------------------------
+  for (int b = tid; b < B; b += blockDim.x) {
+    int len, nchunks, hw = 0;
+    if (!RING) {
+      int ctx = a.context_lens[b];
+      const int lim = a.max_blocks * a.block_size;
+      if (ctx < 0 || ctx > lim) {
+        atomicOr(a.err, PKV_DEVERR_CONTEXT);
+        ctx = ctx < 0 ? 0 : lim;
+      }
+      len = ctx;
+      nchunks = (ctx + kChunk - 1) / kChunk;
+    } else {
+      long long Lb = a.logical_len[b], hb = a.high_water[b];
+      if (Lb < 0 || Lb > 0x3fffffffLL) { atomicOr(a.err, PKV_DEVERR_CONTEXT); Lb = Lb < 0 ? 0 : 0x3fffffff; }
+      if (hb < Lb) hb = Lb;
+      if (hb > 0x3fffffffLL) hb = 0x3fffffff;
+      len = static_cast<int>(Lb);
+      hw = static_cast<int>(hb);
+      nchunks = (min(hw, cap) + kChunk - 1) / kChunk;
+    }
+    slen[b] = len;
+    shw[b] = hw;
+    pre[b + 1] = nchunks;  // scanned below
+  }
+  // zero both Q buffers so rows past R are finite; TMA overwrites rows < R
+  for (int i = tid; i < L::kQBuf * 2 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + L::kQ)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar_full + s * 8, 1);
+      mbar_init(bar_empty + s * 8, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_qfull + s * 8, 1);
+      mbar_init(bar_qempty + s * 8, NCW);
+    }
+    *abort = 0;
+    pre[0] = 0;
+  }
+  fence_barrier_init();
+  __syncthreads();
+  // inclusive scan of chunk counts (warp 0: contiguous slices per lane + shuffle scan)
+  if (warp == 0) {
+    const int per_lane = (B + 31) / 32;
+    const int lo = min(B, lane * per_lane), hi = min(B, lo + per_lane);
+    int sum = 0;
+    for (int b = lo; b < hi; ++b) sum += pre[b + 1];
+    int incl = sum;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int b = lo; b < hi; ++b) {
+      run += pre[b + 1];
+      pre[b + 1] = run;
+    }
+  }
+  __syncthreads();
+
+  const int total = pre[B] * a.Hkv;
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  const int begin = blockIdx.x * per;
+  const Cursor cur{pre, B, a.Hkv, min(total, begin + per)};
+
+  // sequences without any chunk get zeros (their units are in no CTA's slice)
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    if (pre[b + 1] != pre[b]) continue;
+    const int n = a.q_len * a.Hq * kD;
+    for (int i = tid; i < n; i += blockDim.x)
+      a.out[static_cast<int64_t>(b) * n + i] = __float2half_rn(0.f);
+  }
+
+  if (warp == NCW) {
+    // =================================== producer ============================================
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmQ);
+    }
+    const int chunk_mask = (1 << a.bs_shift) - 1;
+    int j = 0, k = 0;
+    Seg s;
+    bool has = cur.first(begin, s);
+    while (has) {
+      if (lane == 0) {
+        const int qs = k & 1;
+        if (k >= 2 && !mbar_wait(bar_qempty + qs * 8, ((k >> 1) - 1) & 1, abort))
+          flag_timeout(a, abort);
+        mbar_arrive_expect_tx(bar_qfull + qs * 8, a.R * 256);
+        const uint32_t qdst = sbase + L::kQ + qs * L::kQBuf;
+        tma_load_3d(qdst, &tmQ, 0, s.h * a.G, s.b * a.q_len, bar_qfull + qs * 8);
+        tma_load_3d(qdst + L::kQHalf, &tmQ, 64, s.h * a.G, s.b * a.q_len, bar_qfull + qs * 8);
+      }
+      const int32_t* bt = a.block_tables + static_cast<int64_t>(s.b) * a.max_blocks;
+      for (int cb = s.c0; cb < s.c1; cb += 32) {
+        const int cc = cb + lane;
+        int row = -kChunk;  // an out-of-range box: TMA fills it with zeros
+        if (cc < s.c1) {
+          const int32_t phys = __ldg(bt + (cc >> a.bs_shift));
+          if (phys >= 0 && phys < a.num_blocks)
+            row = (phys * a.Hkv + s.h) * a.block_size + ((cc & chunk_mask) << 4);
+          else
+            atomicOr(a.err, PKV_DEVERR_BLOCK_ID);
+        }
+        const int n = min(32, s.c1 - cb);
+        for (int l = 0; l < n; ++l, ++j) {
+          const int r = __shfl_sync(0xffffffffu, row, l);
+          if (lane == 0) {
+            const int st = j % NST;
+            if (j >= NST && !mbar_wait(bar_empty + st * 8, ((j / NST) - 1) & 1, abort))
+              flag_timeout(a, abort);
+            const uint32_t fb = bar_full + st * 8;
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            const uint32_t dst = sbase + st * kStageBytes;
+            tma_load_2d(dst, &tmK, 0, r, fb);
+            tma_load_2d(dst + kHalfBytes, &tmK, 64, r, fb);
+            tma_load_2d(dst + 2 * kHalfBytes, &tmV, 0, r, fb);
+            tma_load_2d(dst + 3 * kHalfBytes, &tmV, 64, r, fb);
+          }
+        }
+      }
+      ++k;
+      has = cur.next(s);
+    }
+    // Before exiting, make sure no TMA write into this CTA's shared memory is still pending
+    // (only matters if the consumers gave up early; otherwise these waits return at once).
+    if (lane == 0) {
+      for (int jj = max(0, j - NST); jj < j; ++jj)
+        if (!mbar_wait(bar_full + (jj % NST) * 8, (jj / NST) & 1, nullptr)) flag_timeout(a, abort);
+      for (int kk = max(0, k - 2); kk < k; ++kk)
+        if (!mbar_wait(bar_qfull + (kk & 1) * 8, (kk >> 1) & 1, nullptr)) flag_timeout(a, abort);
+    }
+    return;
+  }
+
+  // ===================================== consumers =============================================
+  const int w = warp;
+  const int g = lane >> 2, t4 = lane & 3;
+  int j = 0, k = 0;
+  Seg s;
+  bool has = cur.first(begin, s);
+  bool first_seg = true;
+  while (has) {
+    const int qs = k & 1;
+    const uint32_t qb = sbase + L::kQ + qs * L::kQBuf;
+    if (!mbar_wait(bar_qfull + qs * 8, (k >> 1) & 1, abort)) flag_timeout(a, abort);
+
+    const int Lc = slen[s.b];  // tokens in cache (paged ctx / ring L)
+    int lo_pos = 0, r_lo = 0;
+    if (RING) {
+      const int hw = shw[s.b];
+      lo_pos = max(a.sink, hw - a.window);
+      r_lo = a.sink + (lo_pos - a.sink) % a.window;
+      // rotate this segment's query rows in place by their own cache index
+      for (int idx = tid; idx < a.R * 64; idx += kNC) {
+        const int r = idx >> 6, d = idx & 63;
+        const int pos = Lc - a.q_len + r / a.G;
+        int jq = pos < a.sink ? pos : a.sink + (pos - lo_pos);
+        jq = min(max(jq, 0), cap - 1);
+        const uint32_t off = swz128(r, d >> 3) + (d & 7) * 2;
+        __half* px = reinterpret_cast<__half*>(smem + (qb - sbase) + off);
+        __half* py = reinterpret_cast<__half*>(smem + (qb - sbase) + L::kQHalf + off);
+        const float2 cs = __ldg(reinterpret_cast<const float2*>(a.rope) + jq * 64 + d);
+        const float x = __half2float(*px), y = __half2float(*py);
+        *px = __float2half_rn(x * cs.x - y * cs.y);
+        *py = __float2half_rn(y * cs.x + x * cs.y);
+      }
+      named_barrier_sync(1, kNC);
+    }
+
+    // Q fragments (A operand, 16 rows x 128 dims per m-tile)
+    uint32_t qf[MT == 1 ? 8 : 1][4];
+    auto q_frag = [&](int mt, int s8, uint32_t (&f)[4]) {
+      const int i = lane >> 3;
+      const int row = mt * 16 + (i & 1) * 8 + (lane & 7);
+      const int ch = 2 * s8 + (i >> 1);
+      ldsm_x4(qb + (ch >> 3) * L::kQHalf + swz128(row, ch & 7), f[0], f[1], f[2], f[3]);
+    };
+    if (MT == 1) {
+#pragma unroll
+      for (int s8 = 0; s8 < 8; ++s8) q_frag(0, s8, qf[s8]);
+      if (RING) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
+    }
+
+    float m_run[MT][2], l_run[MT][2], o[MT][16][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      m_run[mt][0] = m_run[mt][1] = kNegInf;
+      l_run[mt][0] = l_run[mt][1] = 0.f;
+#pragma unroll
+      for (int nd = 0; nd < 16; ++nd) o[mt][nd][0] = o[mt][nd][1] = o[mt][nd][2] = o[mt][nd][3] = 0.f;
+    }
+    // causal limit of each of this thread's rows: query qi sees positions < Lc - q_len + qi + 1
+    int lim[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        const int r = mt * 16 + rh * 8 + g;
+        const int qi = r < a.R ? r / a.G : a.q_len - 1;
+        lim[mt][rh] = Lc - a.q_len + qi + 1;
+      }
+
+    const int nchunk = s.c1 - s.c0;
+    for (int jj = w; jj < nchunk; jj += NCW) {
+      const int gj = j + jj;
+      const int st = gj % NST;
+      if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
+      const uint32_t stK = sbase + st * kStageBytes;
+      const uint32_t stV = stK + 2 * kHalfBytes;
+      const int c = s.c0 + jj;
+
+      // positions of this thread's score columns (tokens nt*8 + 2*t4 + e) and of its K rows
+      int pcol[2][2];
+      int jk[2] = {0, 0};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = c * kChunk + nt * 8 + 2 * t4 + e;
+          if (!RING) {
+            pcol[nt][e] = t;
+          } else {
+            int p;
+            if (t < a.sink) p = t;
+            else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; p = lo_pos + d; }
+            else p = 0x7fffffff;
+            pcol[nt][e] = p;
+          }
+        }
+        if (RING) {
+          const int t = c * kChunk + nt * 8 + g;
+          if (t < a.sink) jk[nt] = t;
+          else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; jk[nt] = a.sink + d; }
+        }
+      }
+      // whole chunk visible to every query row?
+      bool full_chunk;
+      if (!RING) full_chunk = (c + 1) * kChunk <= Lc - a.q_len + 1;
+      else full_chunk = false;
+
+      // ---- S = Q K^T ----
+      float sc[MT][2][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        uint32_t kf[8][2];
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp) {
+          const int ch = 4 * sp + (lane >> 3);
+          const int tok = nt * 8 + (lane & 7);
+          ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), kf[2 * sp][0],
+                  kf[2 * sp][1], kf[2 * sp + 1][0], kf[2 * sp + 1][1]);
+        }
+        if (RING) {
+          // rotate-half RoPE on this thread's key row (token nt*8 + g) by its cache index
+          const float4* tab = reinterpret_cast<const float4*>(a.rope) + jk[nt] * 32;
+#pragma unroll
+          for (int sp = 0; sp < 4; ++sp)
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) {
+              const int d0 = 16 * sp + 8 * ri + 2 * t4;      // even; partner dims d0 + 64
+              const float4 cs = __ldg(tab + (d0 >> 1));
+              const float2 x = __half22float2(*reinterpret_cast<__half2*>(&kf[sp][ri]));
+              const float2 y = __half22float2(*reinterpret_cast<__half2*>(&kf[sp + 4][ri]));
+              kf[sp][ri] = pack_half2(x.x * cs.x - y.x * cs.y, x.y * cs.z - y.y * cs.w);
+              kf[sp + 4][ri] = pack_half2(y.x * cs.x + x.x * cs.y, y.y * cs.z + x.y * cs.w);
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int s8 = 0; s8 < 8; ++s8) {
+            if (MT == 1) {
+              mma_16816(sc[mt][nt], qf[s8][0], qf[s8][1], qf[s8][2], qf[s8][3], kf[s8][0], kf[s8][1]);
+            } else {
+              uint32_t f[4];
+              q_frag(mt, s8, f);
+              mma_16816(sc[mt][nt], f[0], f[1], f[2], f[3], kf[s8][0], kf[s8][1]);
+            }
+          }
+      }
+
+      // ---- mask, online softmax (exp2 domain) ----
+      uint32_t pa[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          float v[4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float x = sc[mt][nt][rh * 2 + e] * a.scale_log2;
+              v[nt * 2 + e] = (full_chunk || pcol[nt][e] < lim[mt][rh]) ? x : kNegInf;
+            }
+          float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float m_new = fmaxf(m_run[mt][rh], mx);
+          const float m_use = m_new == kNegInf ? 0.f : m_new;
+          const float alpha = fast_exp2(m_run[mt][rh] - m_use);
+          m_run[mt][rh] = m_new;
+          float rs = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[i] = fast_exp2(v[i] - m_use);
+            rs += v[i];
+          }
+          l_run[mt][rh] = l_run[mt][rh] * alpha + rs;
+#pragma unroll
+          for (int nd = 0; nd < 16; ++nd) {
+            o[mt][nd][rh * 2] *= alpha;
+            o[mt][nd][rh * 2 + 1] *= alpha;
+          }
+          // P as the A operand: a0/a2 hold row g, a1/a3 row g+8
+          pa[mt][rh] = pack_half2(v[0], v[1]);
+          pa[mt][2 + rh] = pack_half2(v[2], v[3]);
+        }
+      }
+
+      // tokens no query may see (past the cache, or not in the ring's valid set) may hold
+      // anything, NaN included: zero their V entries so that 0 * V stays 0
+      uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+      if (!full_chunk) {
+        const int all = Lc;  // the last query's limit
+        vm0 = (pcol[0][0] < all ? 0x0000ffffu : 0u) | (pcol[0][1] < all ? 0xffff0000u : 0u);
+        vm1 = (pcol[1][0] < all ? 0x0000ffffu : 0u) | (pcol[1][1] < all ? 0xffff0000u : 0u);
+      }
+
+      // ---- O += P V ----
+#pragma unroll
+      for (int np = 0; np < 8; ++np) {
+        const int i = lane >> 3;
+        const int tok = (i & 1) * 8 + (lane & 7);
+        const int ch = 2 * np + (i >> 1);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(stV + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), v0, v1, v2, v3);
+        v0 &= vm0; v1 &= vm1; v2 &= vm0; v3 &= vm1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          mma_16816(o[mt][2 * np], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v0, v1);
+          mma_16816(o[mt][2 * np + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + st * 8);
+    }
+    if (MT != 1) {
+      if (RING) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
+    }
+    j += nchunk;
+
+    // ---- merge the warps' states for this segment ----
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        float lv = l_run[mt][rh];
+        lv += __shfl_xor_sync(0xffffffffu, lv, 1);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 2);
+        const int r = mt * 16 + rh * 8 + g;
+        if (r < a.R) {
+          float* dst = sO + (w * a.R + r) * kD + 2 * t4;
+#pragma unroll
+          for (int nd = 0; nd < 16; ++nd)
+            *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[mt][nd][rh * 2], o[mt][nd][rh * 2 + 1]);
+          if (t4 == 0) {
+            sM[w * a.R + r] = m_run[mt][rh];
+            sL[w * a.R + r] = lv;
+          }
+        }
+      }
+    named_barrier_sync(1, kNC);
+    if (tid < a.R) {
+      float ms = kNegInf;
+      for (int ww = 0; ww < NCW; ++ww) ms = fmaxf(ms, sM[ww * a.R + tid]);
+      float ls = 0.f;
+      if (ms != kNegInf)
+        for (int ww = 0; ww < NCW; ++ww) ls += sL[ww * a.R + tid] * fast_exp2(sM[ww * a.R + tid] - ms);
+      const float inv = ls > 0.f ? 1.f / ls : 0.f;
+      for (int ww = 0; ww < NCW; ++ww)
+        sW[ww * a.R + tid] = ms == kNegInf ? 0.f : fast_exp2(sM[ww * a.R + tid] - ms) * inv;
+      sRow[2 * tid] = ms;
+      sRow[2 * tid + 1] = ls;
+    }
+    named_barrier_sync(1, kNC);
+
+    const bool complete = (s.c0 == 0 && s.c1 == s.nb);
+    const int slot = 2 * blockIdx.x + (first_seg ? 0 : 1);
+    for (int idx = tid; idx < a.R * kD; idx += kNC) {
+      const int r = idx >> 7, d = idx & (kD - 1);
+      float acc = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < NCW; ++ww) acc += sO[(ww * a.R + r) * kD + d] * sW[ww * a.R + r];
+      if (complete) {
+        const int qi = r / a.G, gg = r - qi * a.G;
+        a.out[((static_cast<int64_t>(s.b) * a.q_len + qi) * a.Hq + s.h * a.G + gg) * kD + d] =
+            __float2half_rn(acc);
+      } else {
+        a.part_o[(static_cast<int64_t>(slot) * a.R + r) * kD + d] = acc;
+      }
+    }
+    if (!complete) {
+      if (tid < a.R) {
+        a.part_ml[(static_cast<int64_t>(slot) * a.R + tid) * 2] = sRow[2 * tid];
+        a.part_ml[(static_cast<int64_t>(slot) * a.R + tid) * 2 + 1] = sRow[2 * tid + 1];
+      }
+      __threadfence();
+      named_barrier_sync(1, kNC);
+      const int ua = pre[s.b] * a.Hkv + s.h * s.nb;  // stream index of the unit's first chunk
+      const int cf = ua / per, cl = (ua + s.nb - 1) / per;
+      if (tid == 0) {
+        const int old = atomicAdd(a.counters + s.b * a.Hkv + s.h, 1);
+        *bcast = (old == cl - cf);
+      }
+      named_barrier_sync(1, kNC);
+      if (*bcast) {
+        // last to arrive: merge the unit's partials in slice order
+        __threadfence();
+        if (tid < a.R) {
+          float ms = kNegInf;
+          for (int cc = cf; cc <= cl; ++cc) {
+            const int sl = 2 * cc + ((cc == cf && ua != cc * per) ? 1 : 0);
+            ms = fmaxf(ms, ld_cg_f32(a.part_ml + (static_cast<int64_t>(sl) * a.R + tid) * 2));
+          }
+          float ls = 0.f;
+          if (ms != kNegInf)
+            for (int cc = cf; cc <= cl; ++cc) {
+              const int sl = 2 * cc + ((cc == cf && ua != cc * per) ? 1 : 0);
+              const float* ml = a.part_ml + (static_cast<int64_t>(sl) * a.R + tid) * 2;
+              ls += ld_cg_f32(ml + 1) * fast_exp2(ld_cg_f32(ml) - ms);
+            }
+          sRow[2 * tid] = ms;
+          sRow[2 * tid + 1] = ls > 0.f ? 1.f / ls : 0.f;
+        }
+        named_barrier_sync(1, kNC);
+        for (int idx = tid; idx < a.R * kD; idx += kNC) {
+          const int r = idx >> 7, d = idx & (kD - 1);
+          const float ms = sRow[2 * r], inv = sRow[2 * r + 1];
+          float acc = 0.f;
+          if (ms != kNegInf)
+            for (int cc = cf; cc <= cl; ++cc) {
+              const int sl = 2 * cc + ((cc == cf && ua != cc * per) ? 1 : 0);
+              const float* ml = a.part_ml + (static_cast<int64_t>(sl) * a.R + r) * 2;
+              const float wgt = ld_cg_f32(ml + 1) * fast_exp2(ld_cg_f32(ml) - ms);
+              acc += wgt * ld_cg_f32(a.part_o + (static_cast<int64_t>(sl) * a.R + r) * kD + d);
+            }
+          const int qi = r / a.G, gg = r - qi * a.G;
+          a.out[((static_cast<int64_t>(s.b) * a.q_len + qi) * a.Hq + s.h * a.G + gg) * kD + d] =
+              __float2half_rn(acc * inv);
+        }
+        if (tid == 0) a.counters[s.b * a.Hkv + s.h] = 0;
+      }
+    }
+    named_barrier_sync(1, kNC);  // scratch is reused by the next segment
+    first_seg = false;
+    ++k;
+    has = cur.next(s);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side.
+constexpr int kNCW = 4;
+constexpr int kNST = 8;
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, DecodeArgs);
+
+struct Variant {
+  const void* fn;
+  int mt;
+  bool ring;
+};
+
+template <int MT, bool RING>
+Variant variant() {
+  return Variant{reinterpret_cast<const void*>(&decode_kernel<kNCW, kNST, MT, RING>), MT, RING};
+}
+
+size_t smem_bytes(int mt, int R, int B) {
+  return mt == 1 ? Smem<kNCW, kNST, 1>::bytes(R, B) : Smem<kNCW, kNST, 2>::bytes(R, B);
+}
+
+// Persistent grid for a variant: SM count x resident CTAs (capped), cached per device/size.
+int grid_size(const Variant& v, size_t smem, int* status) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, size_t>, int> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { *status = cuda_status(e); return 0; }
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_tuple(dev, v.fn, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  int occ = 0;
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, (kNCW + 1) * 32, smem);
+  if (e != cudaSuccess) { *status = cuda_status(e); return 0; }
+  if (occ < 1) { *status = PKV_EINVAL; return 0; }
+  const int grid = sm_count() * std::min(occ, kMaxCtasPerSm);
+  cache[key] = grid;
+  return grid;
+}
+
+struct WsLayout {
+  size_t counters, part_ml, part_o, total;
+};
+
+WsLayout ws_layout(int num_seqs, int Hkv, int R) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t partials = static_cast<size_t>(2) * sm_count() * kMaxCtasPerSm;
+  WsLayout w;
+  w.counters = 0;
+  w.part_ml = up(static_cast<size_t>(num_seqs) * Hkv * sizeof(int));
+  w.part_o = w.part_ml + up(partials * R * 2 * sizeof(float));
+  w.total = w.part_o + up(partials * R * kD * sizeof(float));
+  return w;
+}
+
+int encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+           const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return PKV_ECUDA_BASE - static_cast<int>(cudaErrorNotSupported);
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_EINVAL;
+}
+
+int launch_decode(bool ring, void* out, const void* q, const void* k_cache, const void* v_cache,
+                  int num_blocks, const int32_t* block_tables, int max_blocks,
+                  const int32_t* context_lens, const int64_t* logical_len,
+                  const int64_t* high_water, int num_seqs, int q_len, int Hq, int Hkv,
+                  int head_dim, int block_size, int sink, int window, const float* rope,
+                  float scale, void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_seqs < 0 || q_len < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || head_dim != kD ||
+      !valid_block_size(block_size) || num_blocks < 0 || max_blocks < 0)
+    return PKV_EINVAL;
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > kMaxSeqs) return PKV_EINVAL;
+  const int G = Hq / Hkv;
+  const int R = G * q_len;
+  if (R > 32) return PKV_EINVAL;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !workspace) return PKV_EINVAL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PKV_EINVAL;
+  if (ring) {
+    if (!logical_len || !high_water || !rope || sink < 0 || window < 1) return PKV_EINVAL;
+    if ((sink + window + block_size - 1) / block_size > max_blocks) return PKV_EINVAL;
+  } else if (!context_lens) {
+    return PKV_EINVAL;
+  }
+  // all chunk indices and TMA rows fit in int32
+  const int64_t rows = static_cast<int64_t>(num_blocks) * Hkv * block_size;
+  const int64_t max_ctx = ring ? (sink + window) : static_cast<int64_t>(max_blocks) * block_size;
+  if (rows >= (1ll << 31) || static_cast<int64_t>(num_seqs) * Hkv * ((max_ctx + kChunk - 1) / kChunk) >= (1ll << 30))
+    return PKV_EINVAL;
+  if (num_blocks == 0) return PKV_EINVAL;
+  const WsLayout ws = ws_layout(num_seqs, Hkv, R);
+  if (workspace_bytes < ws.total) return PKV_ENOSPC;
+
+  const int mt = R <= 16 ? 1 : 2;
+  Variant v = ring ? (mt == 1 ? variant<1, true>() : variant<2, true>())
+                   : (mt == 1 ? variant<1, false>() : variant<2, false>());
+  const size_t smem = smem_bytes(mt, R, num_seqs);
+  if (smem > 227 * 1024) return PKV_EINVAL;
+  int status = PKV_OK;
+  const int grid = grid_size(v, smem, &status);
+  if (!grid) return status != PKV_OK ? status : PKV_EINVAL;
+
+  CUtensorMap tmK, tmV, tmQ;
+  const cuuint64_t kv_dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t kv_strides[1] = {kD * 2};
+  const cuuint32_t kv_box[2] = {64, kChunk};
+  int st = encode(&tmK, k_cache, 2, kv_dims, kv_strides, kv_box);
+  if (st == PKV_OK) st = encode(&tmV, v_cache, 2, kv_dims, kv_strides, kv_box);
+  const cuuint64_t q_dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(Hq),
+                                static_cast<cuuint64_t>(num_seqs) * q_len};
+  const cuuint64_t q_strides[2] = {kD * 2, static_cast<cuuint64_t>(Hq) * kD * 2};
+  const cuuint32_t q_box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(q_len)};
+  if (st == PKV_OK) st = encode(&tmQ, q, 3, q_dims, q_strides, q_box);
+  if (st != PKV_OK) return st;
+
+  unsigned int* err = device_error_ptr();
+  if (!err) return cuda_status(cudaGetLastError());
+  DecodeArgs args;
+  args.out = static_cast<__half*>(out);
+  args.block_tables = block_tables;
+  args.context_lens = context_lens;
+  args.logical_len = logical_len;
+  args.high_water = high_water;
+  args.rope = rope;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  args.counters = reinterpret_cast<int*>(wsb + ws.counters);
+  args.part_ml = reinterpret_cast<float*>(wsb + ws.part_ml);
+  args.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
+  args.err = err;
+  args.num_blocks = num_blocks;
+  args.max_blocks = max_blocks;
+  args.num_seqs = num_seqs;
+  args.q_len = q_len;
+  args.Hq = Hq;
+  args.Hkv = Hkv;
+  args.G = G;
+  args.R = R;
+  args.block_size = block_size;
+  int shift = 0;
+  while ((kChunk << shift) < block_size) ++shift;
+  args.bs_shift = shift;
+  args.sink = sink;
+  args.window = window;
+  args.scale_log2 = scale * 1.4426950408889634f;
+
+  void* params[4] = {&tmK, &tmV, &tmQ, &args};
+  cudaError_t e = cudaLaunchKernel(v.fn, dim3(grid), dim3((kNCW + 1) * 32), params, smem,
+                                   static_cast<cudaStream_t>(stream));
+  return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                  int head_dim) {
+  if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 ||
+      num_q_heads % num_kv_heads || head_dim != kD || sm_count() == 0)
+    return 0;
+  const int R = num_q_heads / num_kv_heads * q_len;
+  return ws_layout(std::max(num_seqs, 1), num_kv_heads, R).total;
+}
+
+int pkv_workspace_init(void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  if (!workspace) return PKV_EINVAL;
+  return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int pkv_paged_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          int num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int num_seqs, int q_len, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size, float scale,
+                          void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  return launch_decode(false, out, q, k_cache, v_cache, num_blocks, block_tables,
+                       max_blocks_per_seq, context_lens, nullptr, nullptr, num_seqs, q_len,
+                       num_q_heads, num_kv_heads, head_dim, block_size, 0, 1, nullptr, scale,
+                       workspace, workspace_bytes, stream);
+}
+
+int pkv_ring_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         int num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
+                         const int64_t* logical_len, const int64_t* high_water, int num_seqs,
+                         int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int sink, int window, const float* rope_cos_sin,
+                         float scale, void* workspace, size_t workspace_bytes,
+                         pkv_stream_t stream) {
+  return launch_decode(true, out, q, k_cache, v_cache, num_blocks, block_tables,
+                       max_blocks_per_seq, nullptr, logical_len, high_water, num_seqs, q_len,
+                       num_q_heads, num_kv_heads, head_dim, block_size, sink, window,
+                       rope_cos_sin, scale, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

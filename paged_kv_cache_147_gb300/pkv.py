@@ -1,0 +1,220 @@
+"""Thin Python binding of libpkv.so (the C ABI declared in include/pkv.h).
+
+Each function has the name of its C entry point without the ``pkv_`` prefix and only
+marshals arguments: it reads shapes and device pointers off torch tensors, passes the
+current CUDA stream, and turns a negative status into :class:`PkvError`. Every step of the
+computation runs in the library's CUDA kernels; there is no fallback path. Loading fails
+loudly if the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+# Symbols the header declares (kept in sync with include/pkv.h; the CPU tests check both).
+SYMBOLS = (
+    "pkv_version", "pkv_device_error", "pkv_slot_mapping", "pkv_ring_slot_mapping",
+    "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes", "pkv_workspace_init",
+    "pkv_paged_attn_decode", "pkv_rope_table", "pkv_ring_attn_decode", "pkv_check_tables",
+    "pkv_check_slots",
+)
+
+OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
+DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_SEQ, DEVERR_POSITION = \
+    1, 2, 4, 8, 16, 32
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        if status <= ECUDA_BASE:
+            what = f"CUDA error {ECUDA_BASE - status}"
+        else:
+            what = {EINVAL: "invalid argument", ERANGE: "index out of range",
+                    ENOSPC: "workspace too small"}.get(status, "error")
+        super().__init__(f"{fn} failed: {what} (status {status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Loads libpkv.so (built by paged_kv_cache_147_gb300.build); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m paged_kv_cache_147_gb300.build` (no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, sz, f32, f64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                     ctypes.c_size_t, ctypes.c_float, ctypes.c_double)
+        sig = {
+            "pkv_version": (i32, []),
+            "pkv_device_error": (i32, [P, i32, P]),
+            "pkv_slot_mapping": (i32, [P, P, i32, P, i32, i32, i32, P, P]),
+            "pkv_ring_slot_mapping": (i32, [P, P, i32, P, i32, i32, i32, i32, i32, P, P]),
+            "pkv_kv_append": (i32, [P, P, P, i32, P, P, i32, i32, i32, i32, P]),
+            "pkv_copy_blocks": (i32, [P, P, P, P, i32, i64, i32, i32, i32, i32, i32, P]),
+            "pkv_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
+            "pkv_workspace_init": (i32, [P, sz, P]),
+            "pkv_paged_attn_decode": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32,
+                                            i32, f32, P, sz, P]),
+            "pkv_rope_table": (i32, [P, i32, i32, f64]),
+            "pkv_ring_attn_decode": (i32, [P, P, P, P, i32, P, i32, P, P, i32, i32, i32, i32,
+                                           i32, i32, i32, i32, P, f32, P, sz, P]),
+            "pkv_check_tables": (i32, [P, P, i32, i32, i32, i32, P]),
+            "pkv_check_slots": (i32, [P, i32, i32, i32, P]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype, f.argtypes = res, args
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != OK:
+        raise PkvError(fn, status)
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _p(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def version() -> int:
+    return load().pkv_version()
+
+
+def device_error(clear: bool = True, stream=None) -> int:
+    out = ctypes.c_uint(0)
+    _check("pkv_device_error", load().pkv_device_error(ctypes.byref(out), int(clear),
+                                                        _stream(stream)))
+    return out.value
+
+
+# ------------------------------------------------------------------------------ slot mapping
+def slot_mapping(seq_ids, positions, block_tables, block_size, out=None, stream=None):
+    n = positions.numel()
+    out = torch.empty(n, dtype=torch.int64, device=positions.device) if out is None else out
+    _check("pkv_slot_mapping", load().pkv_slot_mapping(
+        _p(seq_ids), _p(positions), n, _p(block_tables), block_tables.shape[0],
+        block_tables.shape[1], block_size, _p(out), _stream(stream)))
+    return out
+
+
+def ring_slot_mapping(seq_ids, positions, block_tables, sink, window, block_size, out=None,
+                      stream=None):
+    n = positions.numel()
+    out = torch.empty(n, dtype=torch.int64, device=positions.device) if out is None else out
+    _check("pkv_ring_slot_mapping", load().pkv_ring_slot_mapping(
+        _p(seq_ids), _p(positions), n, _p(block_tables), block_tables.shape[0],
+        block_tables.shape[1], sink, window, block_size, _p(out), _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------------------ cache edits
+def kv_append(k, v, slots, k_cache, v_cache, stream=None):
+    """k, v [T, Hkv, D]; k_cache, v_cache one layer [NB, Hkv, bs, D]."""
+    nb, hkv, bs, d = k_cache.shape
+    _check("pkv_kv_append", load().pkv_kv_append(
+        _p(k), _p(v), _p(slots), slots.numel(), _p(k_cache), _p(v_cache), nb, hkv, d, bs,
+        _stream(stream)))
+
+
+def copy_blocks(k_cache, v_cache, src, dst, stream=None):
+    """k_cache, v_cache [layers, NB, Hkv, bs, D] (or one layer [NB, Hkv, bs, D])."""
+    kc = k_cache if k_cache.dim() == 5 else k_cache.unsqueeze(0)
+    layers, nb, hkv, bs, d = kc.shape
+    _check("pkv_copy_blocks", load().pkv_copy_blocks(
+        _p(k_cache), _p(v_cache), _p(src), _p(dst), src.numel(), kc.stride(0), layers, nb, hkv,
+        d, bs, _stream(stream)))
+
+
+# ------------------------------------------------------------------------------ attention
+def decode_workspace_bytes(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim=128) -> int:
+    n = load().pkv_decode_workspace_bytes(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim)
+    if n == 0:
+        raise PkvError("pkv_decode_workspace_bytes", EINVAL)
+    return int(n)
+
+
+def workspace_init(workspace, stream=None):
+    _check("pkv_workspace_init", load().pkv_workspace_init(
+        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def make_workspace(num_seqs, q_len, num_q_heads, num_kv_heads, device="cuda", stream=None):
+    """Allocates (through torch) and zeroes a decode workspace."""
+    ws = torch.empty(decode_workspace_bytes(num_seqs, q_len, num_q_heads, num_kv_heads),
+                     dtype=torch.uint8, device=device)
+    workspace_init(ws, stream)
+    return ws
+
+
+def paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, workspace,
+                      stream=None):
+    """q, out [B, q_len, Hq, D]; k_cache, v_cache one layer [NB, Hkv, bs, D]."""
+    B, q_len, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_paged_attn_decode", load().pkv_paged_attn_decode(
+        _p(out), _p(q), _p(k_cache), _p(v_cache), nb, _p(block_tables), block_tables.shape[1],
+        _p(context_lens), B, q_len, hq, hkv, d, bs, float(scale), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def rope_table(n_index, head_dim=128, base=10000.0) -> torch.Tensor:
+    """Host float32 [n_index, head_dim/2, 2] (cos, sin) table; move it to the device."""
+    t = torch.empty((n_index, head_dim // 2, 2), dtype=torch.float32)
+    _check("pkv_rope_table", load().pkv_rope_table(_p(t), n_index, head_dim, float(base)))
+    return t
+
+
+def ring_attn_decode(out, q, k_cache, v_cache, block_tables, logical_len, high_water, sink,
+                     window, rope_cos_sin, scale, workspace, stream=None):
+    B, q_len, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_ring_attn_decode", load().pkv_ring_attn_decode(
+        _p(out), _p(q), _p(k_cache), _p(v_cache), nb, _p(block_tables), block_tables.shape[1],
+        _p(logical_len), _p(high_water), B, q_len, hq, hkv, d, bs, sink, window,
+        _p(rope_cos_sin), float(scale), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------------------ host checks
+def check_tables(block_tables, context_lens, block_size, num_blocks) -> int | None:
+    """Host validation; returns None if valid, else the first bad sequence index."""
+    bt = block_tables.detach().to("cpu", torch.int32).contiguous()
+    cl = context_lens.detach().to("cpu", torch.int32).contiguous()
+    bad = ctypes.c_int(-1)
+    st = load().pkv_check_tables(_p(bt), _p(cl), bt.shape[0], bt.shape[1], block_size,
+                                 num_blocks, ctypes.byref(bad))
+    if st == ERANGE:
+        return bad.value
+    _check("pkv_check_tables", st)
+    return None
+
+
+def check_slots(slots, num_blocks, block_size) -> int | None:
+    s = slots.detach().to("cpu", torch.int64).contiguous()
+    bad = ctypes.c_int(-1)
+    st = load().pkv_check_slots(_p(s), s.numel(), num_blocks, block_size, ctypes.byref(bad))
+    if st == ERANGE:
+        return bad.value
+    _check("pkv_check_slots", st)
+    return None

@@ -100,6 +100,10 @@ class Workload:
         g = self._gen(layer, tag, device)
         return torch.randn(shape, generator=g, device=device, dtype=torch.float32).half()
 
+    def draw(self, shape, layer: int, tag: int, device="cpu") -> torch.Tensor:
+        """An extra seeded N(0, 1) fp16 tensor (tags >= 100 are free for callers)."""
+        return self._randn(shape, layer, tag, device)
+
     def pools(self, device="cpu", poison: bool = False, layers=None):
         """K and V pools [num_layers, NB, Hkv, bs, D] fp16 (one tensor each, layer-strided).
 
