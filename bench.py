@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark of paged decode attention on one GPU (or N data-parallel replicas).
+
+One step is one decode step of the whole attention stack of the workload: slot mapping of
+the step's new tokens, then for every layer the KV append and the paged decode attention,
+all through the C ABI of libpkv.so, captured once in a CUDA graph and replayed.
+
+Printed (rank 0, one JSON line): the KV-read bandwidth (algorithmic fp16 K+V bytes the step
+reads over the step time), decode tokens/s, the decode kernel's roofline against the
+measured HBM copy peak, the end-to-end figure with host buffers (inputs copied in and the
+attention output copied back every step), the fp64 CPU oracle's rate on a bounded sample of
+the same workload, the SM clocks seen during the timed region and the kernel launch count.
+
+`--impl reference` times the CPU oracle alone (the reference arm): each step is a bounded
+sample of the workload, sized so the whole run ends in a few minutes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_kv_cache_147_gb300 import replicas, workloads  # noqa: E402
+
+METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak), decode tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=30)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="edge_1p1b",
+                    choices=["edge_1p1b", "llama70b_b16", "llama70b_mixed"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def describe(w) -> dict:
+    cl = w.context_lens.astype(np.int64)
+    return {
+        "workload": w.name,
+        "layers": w.num_layers, "num_seqs": w.num_seqs, "q_len": w.q_len,
+        "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+        "block_size": w.block_size, "pool_blocks_per_layer": w.num_blocks,
+        "context_min_mean_max": [int(cl.min()), round(float(cl.mean()), 1), int(cl.max())],
+        "kv_bytes_per_step": w.kv_read_bytes(),
+        "accumulate": "f32",
+        "l2": f"no flush: one step reads {w.kv_read_bytes() / 1e9:.2f} GB of K/V, "
+              f"more than the {L2_BYTES / 2**20:.0f} MiB L2",
+    }
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------ our arm
+class Step:
+    """Device-resident inputs of one decode step and the launches that make it."""
+
+    def __init__(self, w, dev, seed_offset=0):
+        from paged_kv_cache_147_gb300 import pkv
+        self.pkv = pkv
+        self.w = w
+        self.dev = dev
+        Lr = w.num_layers
+        self.k, self.v = w.pools(dev)
+        self.bt = torch.as_tensor(w.block_tables, device=dev)
+        self.cl = torch.as_tensor(w.context_lens, device=dev)
+        seq, pos = w.new_token_positions()
+        self.seq = torch.as_tensor(seq, device=dev)
+        self.pos = torch.as_tensor(pos, device=dev)
+        self.q = torch.stack([w.query(l, dev) for l in range(Lr)])
+        kv = [w.new_kv(l, dev) for l in range(Lr)]
+        self.kn = torch.stack([a for a, _ in kv])
+        self.vn = torch.stack([b for _, b in kv])
+        self.out = torch.empty_like(self.q)
+        self.slots = torch.empty(seq.shape[0], dtype=torch.int64, device=dev)
+        self.ws = pkv.make_workspace(w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, dev)
+        self.launches_per_step = 1 + 2 * Lr
+
+    def run(self):
+        p, w = self.pkv, self.w
+        p.slot_mapping(self.seq, self.pos, self.bt, w.block_size, out=self.slots)
+        for l in range(w.num_layers):
+            p.kv_append(self.kn[l], self.vn[l], self.slots, self.k[l], self.v[l])
+            p.paged_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.cl,
+                                w.scale, self.ws)
+
+    def run_decode_only(self):
+        p, w = self.pkv, self.w
+        for l in range(w.num_layers):
+            p.paged_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.cl,
+                                w.scale, self.ws)
+
+    def h2d_sources(self):
+        return [self.q, self.kn, self.vn, self.bt, self.cl, self.seq, self.pos]
+
+
+def capture(fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()                         # warm the host-side caches outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_replays(g, steps, warmup) -> float:
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    replicas.barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        g.replay()
+    end.record()
+    end.synchronize()
+    torch.cuda.synchronize()
+    replicas.barrier()
+    return start.elapsed_time(end) / 1e3
+
+
+def traffic_record(w):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"paged_decode_{w.name}.traffic.json")
+    src = os.path.join(ROOT, "paged_kv_cache_147_gb300", "csrc", "pkv_decode.cu")
+    try:
+        rec = json.load(open(path))
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if rec.get("source_sha256_16") == digest:
+            return rec.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def run_ours(args, w, rank, local_rank, world_size):
+    dev = f"cuda:{local_rank}"
+    torch.cuda.set_device(local_rank)
+    from paged_kv_cache_147_gb300 import pkv
+    pkv.load()
+    st = Step(w, dev)
+    step_graph = capture(st.run)
+    decode_graph = capture(st.run_decode_only)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    elapsed = time_replays(step_graph, args.steps, args.warmup)
+    clk = clocks.stop()
+    bytes_step = w.kv_read_bytes()
+    t_max, total_bytes = replicas.aggregate(elapsed, float(bytes_step) * args.steps,
+                                            device=dev)
+    value = total_bytes / t_max / 1e9
+
+    # dominant kernel: decode attention, timed alone over the same replays
+    dsteps = max(10, args.steps // 2)
+    d_elapsed = time_replays(decode_graph, dsteps, args.warmup)
+    per_launch = d_elapsed / (dsteps * w.num_layers)
+    bytes_launch = bytes_step / w.num_layers
+    peak, peak_kind = load_peaks()
+    achieved = bytes_launch / per_launch / 1e9
+    traffic = traffic_record(w)
+
+    e2e = None
+    if not args.no_e2e:
+        srcs = st.h2d_sources()
+        host_in = [t.cpu().pin_memory() for t in srcs]
+        host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = host_out.numel() * host_out.element_size()
+
+        def e2e_step():
+            for d, h in zip(srcs, host_in):
+                d.copy_(h, non_blocking=True)
+            step_graph.replay()
+            host_out.copy_(st.out, non_blocking=True)
+
+        esteps = max(5, args.steps // 10)
+        for _ in range(max(3, args.warmup // 3)):
+            e2e_step()
+        torch.cuda.synchronize()
+        replicas.barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(esteps):
+            e2e_step()
+        t1.record()
+        t1.synchronize()
+        e_el, e_bytes = replicas.aggregate(t0.elapsed_time(t1) / 1e3,
+                                           float(bytes_step) * esteps, device=dev)
+        e2e = {"value": round(e_bytes / e_el / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_el / esteps * 1e3, 4),
+               "path": "pinned host inputs -> device, C-ABI step (graph replay), "
+                       "attention output -> pinned host"}
+    dev_err = pkv.device_error(clear=True)
+    if dev_err:
+        raise RuntimeError(f"device error word {dev_err:#x} after the benchmark")
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world_size,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_max / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": describe(w) | {"graph": f"CUDA graph: slot mapping + {w.num_layers} x "
+                                          "(kv_append, paged_attn_decode)",
+                                 "parallelism": f"replicas x{world_size}"},
+        "decode_tokens_per_s": round(w.num_seqs * w.q_len * args.steps * world_size / t_max, 1),
+        "pct_of_nominal_8tbs": round(100 * value / world_size / NOMINAL_HBM_GBS, 2),
+        f"pct_of_{peak_kind}_hbm": round(100 * value / world_size / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_kernel (paged_attn_decode)",
+                     "launch_us": round(per_launch * 1e6, 3),
+                     "algorithmic_bytes_per_launch": int(bytes_launch),
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    return line
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+def oracle_sample(w, seqs, layers):
+    """Runs the oracle's append + attention over `seqs` of each of `layers`; returns
+    (seconds, kv bytes attended, threads used)."""
+    import oracle
+    secs, nbytes, threads = 0.0, 0, 1
+    mask = np.zeros(w.num_seqs, dtype=np.uint8)
+    mask[list(seqs)] = 1
+    seq_ids, pos = w.new_token_positions()
+    for l in layers:
+        k, v = (t.numpy() for t in w.layer_pool(l))
+        q = w.query(l).numpy()
+        kn, vn = (t.numpy() for t in w.new_kv(l))
+        sel = np.isin(seq_ids, np.nonzero(mask)[0])
+        t0 = time.perf_counter()
+        slots = oracle.slot_mapping(seq_ids[sel], pos[sel], w.block_tables, w.block_size)
+        oracle.kv_append(kn[sel], vn[sel], slots, k, v, w.block_size)
+        _, threads = oracle.paged_attention(q, k, v, w.block_tables, w.context_lens,
+                                            w.block_size, w.scale, seq_mask=mask,
+                                            return_threads=True)
+        secs += time.perf_counter() - t0
+        nbytes += int(w.context_lens[mask.astype(bool)].astype(np.int64).sum()) * \
+            w.num_kv_heads * w.head_dim * 4
+    return secs, nbytes, threads
+
+
+def cpu_baseline(w, budget_s):
+    import oracle
+    oracle.build()
+    secs, nbytes, threads = oracle_sample(w, range(w.num_seqs), [0])
+    layers = 1
+    while layers < w.num_layers and secs * (layers + 1) / layers < budget_s:
+        s, b, threads = oracle_sample(w, range(w.num_seqs), [layers])
+        secs, nbytes, layers = secs + s, nbytes + b, layers + 1
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{layers} of {w.num_layers} layers, all {w.num_seqs} sequences "
+                      f"(append + fp64 attention), {secs:.1f} s"}
+
+
+def run_reference(args, w, world_size):
+    import oracle
+    oracle.build()
+    # calibrate: one sequence-sized unit of work, then size each step to fit the budget
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    probe_s, _, _ = oracle_sample(w, range(min(4, w.num_seqs)), [0])
+    per_seq = probe_s / min(4, w.num_seqs)
+    n = int(max(1, min(w.num_seqs, budget / max(per_seq, 1e-6))))
+    rng = np.random.default_rng(0)
+    secs, nbytes, threads = 0.0, 0, 1
+    for i in range(args.warmup + args.steps):
+        seqs = rng.choice(w.num_seqs, size=n, replace=False)
+        s, b, threads = oracle_sample(w, seqs, [i % w.num_layers])
+        if i >= args.warmup:
+            secs, nbytes = secs + s, nbytes + b
+    value = nbytes / secs / 1e9
+    sample = (f"each step: {n} of {w.num_seqs} sequences of one layer (cycling layers), "
+              "append + fp64 attention")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(w),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank, local_rank, world_size = replicas.world()
+    w = workloads.WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w, world_size)), flush=True)
+        return
+    replicas.init()
+    line = run_ours(args, w, rank, local_rank, world_size)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    replicas.shutdown()
+
+
+if __name__ == "__main__":
+    main()

@@ -125,6 +125,11 @@ class Workload:
             v.masked_fill_(mask, float("nan"))
         return k, v
 
+    def layer_pool(self, layer: int, device="cpu"):
+        """One layer's K and V pools [NB, Hkv, bs, D] (the same values pools() puts there)."""
+        shape = self.pool_shape()[1:]
+        return self._randn(shape, layer, 1, device), self._randn(shape, layer, 2, device)
+
     def query(self, layer: int, device="cpu") -> torch.Tensor:
         """q [B, q_len, Hq, D] fp16."""
         return self._randn((self.num_seqs, self.q_len, self.num_q_heads, self.head_dim),
