@@ -36,15 +36,20 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, defines=(), out: str | None = None) -> str:
+    """Compiles libpkv.so. `defines` (e.g. ["PKV_DECODE_STAGES=10"]) and `out` build a
+    variant elsewhere; the default library is rebuilt only when a source is newer."""
+    lib = out or LIB
+    if not force and not defines and out is None and not _stale():
         return LIB
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    bdir = BUILD if out is None else out + ".build"
+    os.makedirs(bdir, exist_ok=True)
     procs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
+        cmd = [nvcc, *ARCH, *FLAGS, *[f"-D{d}" for d in defines], "-c",
+               os.path.join(CSRC, src), "-o", obj]
         procs.append((src, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE,
                                                  stderr=subprocess.STDOUT, text=True)))
     objs = []
@@ -55,14 +60,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if p.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}")
         objs.append(obj)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
         sys.stdout.write(r.stdout)
         raise RuntimeError("linking libpkv.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

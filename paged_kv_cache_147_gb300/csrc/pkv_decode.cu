@@ -58,7 +58,7 @@ struct DecodeArgs {
   const int64_t* high_water;    // ring: hw
   const float* rope;            // ring: [sink + window][64][2] (cos, sin)
   float* part_o;                // [2 * grid][R][128]
-  float* part_ml;               // [2 * grid][R][2]
+  float* part_ml;               // [2 * grid][R][4]: m, l, 0, 0 (16-byte rows)
   int* counters;                // [num_seqs * Hkv]
   unsigned int* err;
   int num_blocks, max_blocks, num_seqs, q_len, Hq, Hkv, G, R;
@@ -80,13 +80,14 @@ struct Smem {
   static constexpr int kQHalf = MT * 2048;            // 16*MT rows x 128 B
   static constexpr int kQBuf = 2 * kQHalf;
   static constexpr int kQ = NST * kStageBytes;
-  static constexpr int kBars = kQ + 2 * kQBuf;        // full[NST], empty[NST], qfull[2], qempty[2]
-  static constexpr int kFlags = kBars + (2 * NST + 4) * 8;  // abort, bcast
-  static constexpr int kScratch = kFlags + 16;
-  __host__ __device__ static int scratch_floats(int R) {  // sO + sM + sL + sW + sRow
-    return NCW * R * kD + 3 * NCW * R + 2 * R;
-  }
-  __host__ __device__ static int seq_off(int R) { return kScratch + scratch_floats(R) * 4; }
+  // full[NST], empty[NST], qfull[2], qempty[2], sdone[2], sfree[2]
+  static constexpr int kBars = kQ + 2 * kQBuf;
+  static constexpr int kFlags = kBars + (2 * NST + 8) * 8;  // abort, pending count + units
+  static constexpr int kState = kFlags + 64;
+  // segment states handed from the consumer warps to the epilogue warp, double-buffered:
+  // o [2][NCW][R][128], m [2][NCW][R], l [2][NCW][R]; then the epilogue's weights [NCW][R]
+  __host__ __device__ static int state_floats(int R) { return 2 * NCW * R * (kD + 2) + NCW * R; }
+  __host__ __device__ static int seq_off(int R) { return kState + state_floats(R) * 4; }
   // per sequence: prefix (B+1 ints), length, high water
   __host__ static size_t bytes(int R, int B) {
     return 1024 + static_cast<size_t>(seq_off(R)) + static_cast<size_t>(3 * B + 1) * 4;
@@ -140,12 +141,172 @@ __device__ __forceinline__ void flag_timeout(const DecodeArgs& a, volatile int* 
 }
 
 // ---------------------------------------------------------------------------------------------
+// Sync of the threads taking part in a merge: one warp, or a named barrier over NT threads.
+template <int NT>
+__device__ __forceinline__ void merge_sync() {
+  if (NT == 32) __syncwarp();
+  else named_barrier_sync(2, NT);
+}
+
+// Output row r (= query token qi, head g of the group) of unit (b, h): pointer to its 128 halves.
+__device__ __forceinline__ __half* out_row(const DecodeArgs& a, int b, int h, int r) {
+  const int qi = r / a.G, gg = r - qi * a.G;
+  return a.out + ((static_cast<int64_t>(b) * a.q_len + qi) * a.Hq + h * a.G + gg) * kD;
+}
+
+__device__ __forceinline__ void store_half4(__half* dst, float4 v) {
+  uint2 u;
+  u.x = pack_half2(v.x, v.y);
+  u.y = pack_half2(v.z, v.w);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+// Merge of one segment's per-warp states (o [NCW][R][128] unnormalised, m and l [NCW][R]) into
+// the unit's output (complete segment) or its normalised partial (split unit), by NT threads
+// t = 0..NT-1. Each thread owns 4 consecutive dims of a row (float4 in, 8 bytes out).
+template <int NCW, int NT>
+__device__ __forceinline__ void merge_segment(const DecodeArgs& a, const float* o_s,
+                                              const float* m_s, const float* l_s, float* ew,
+                                              int b, int h, bool complete, int slot, int t) {
+  const int R = a.R;
+  if (t < R) {
+    float mw[NCW], row_m = kNegInf;
+#pragma unroll
+    for (int ww = 0; ww < NCW; ++ww) {
+      mw[ww] = m_s[ww * R + t];
+      row_m = fmaxf(row_m, mw[ww]);
+    }
+    float row_l = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < NCW; ++ww) {
+      mw[ww] = row_m == kNegInf ? 0.f : fast_exp2(mw[ww] - row_m);
+      row_l += l_s[ww * R + t] * mw[ww];
+    }
+    const float inv = row_l > 0.f ? 1.f / row_l : 0.f;
+#pragma unroll
+    for (int ww = 0; ww < NCW; ++ww) ew[ww * R + t] = mw[ww] * inv;
+    if (!complete)
+      *reinterpret_cast<float4*>(a.part_ml + (static_cast<int64_t>(slot) * R + t) * 4) =
+          make_float4(row_m, row_l, 0.f, 0.f);
+  }
+  merge_sync<NT>();
+#pragma unroll 2
+  for (int gi = t; gi < R * 32; gi += NT) {
+    const int r = gi >> 5, c4 = gi & 31;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int ww = 0; ww < NCW; ++ww) {
+      const float4 v = reinterpret_cast<const float4*>(o_s + (ww * R + r) * kD)[c4];
+      const float wt = ew[ww * R + r];
+      acc.x += wt * v.x; acc.y += wt * v.y; acc.z += wt * v.z; acc.w += wt * v.w;
+    }
+    if (complete)
+      store_half4(out_row(a, b, h, r) + c4 * 4, acc);
+    else
+      reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(slot) * R + r) * kD)[c4] = acc;
+  }
+}
+
+// Merge of a split unit's partials, run cooperatively by NT threads of the last CTA to arrive
+// on the unit's counter, after its whole slice is done (so its pipeline stages are free).
+// Partial p (in slice order) holds per row its max m_p, sum l_p and normalised output o_p; the
+// result is sum_p o_p l_p 2^(m_p - M) / sum_p l_p 2^(m_p - M), M = max_p m_p, formed in slice
+// order. The partials are copied into the stage memory with cp.async (as many per batch as fit,
+// usually all: one round trip to L2); each thread then reduces its own 4 output dims in one
+// pass, recomputing its row's weights, with no barrier inside a batch.
+template <int NT>
+__device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, int nb,
+                                           const int* pre, int per, uint8_t* stage_mem,
+                                           int stage_bytes, int t) {
+  const int R = a.R;
+  const int ua = pre[b] * a.Hkv + h * nb;
+  const int cf = ua / per, cl = (ua + nb - 1) / per;
+  const bool first_odd = ua != cf * per;
+  float* accv = reinterpret_cast<float*>(stage_mem);       // [R][128] running output
+  float* rowml = accv + R * kD;                            // [2][R][2] running (max, sum)
+  uint8_t* rest = reinterpret_cast<uint8_t*>(rowml + 4 * R);
+  const int part_bytes = R * (kD + 4) * 4;                 // o rows and (m, l, -, -) rows
+  const int PB = (stage_bytes - (R * kD + 4 * R) * 4) / part_bytes;   // >= 2
+  float* so = reinterpret_cast<float*>(rest);              // [PB][R][128]
+  float* sml = so + PB * R * kD;                           // [PB][R][4]
+  const uint32_t so_s = smem_u32(so), sml_s = smem_u32(sml);
+  const int o_vec = R * kD / 4;                            // 16-byte pieces of one partial's o
+  int batch = 0;
+#pragma unroll 1
+  for (int base = cf; base <= cl; base += PB, ++batch) {
+    const int nbp = min(PB, cl - base + 1);
+    const bool last_batch = base + PB > cl;
+    merge_sync<NT>();                      // previous batch fully used
+#pragma unroll 4
+    for (int i = t; i < nbp * (o_vec + R); i += NT) {
+      const bool is_o = i < nbp * o_vec;
+      const int j = is_o ? i : i - nbp * o_vec;
+      const int per_part = is_o ? o_vec : R;
+      const int p = j / per_part, off = j - p * per_part;
+      const int cc = base + p;
+      const int64_t sl = 2 * cc + ((cc == cf && first_odd) ? 1 : 0);
+      if (is_o)
+        cp_async_16(so_s + (p * R * kD + off * 4) * 4, a.part_o + sl * R * kD + off * 4);
+      else
+        cp_async_16(sml_s + (p * R + off) * 16, a.part_ml + (sl * R + off) * 4);
+    }
+    cp_async_wait_all();
+    merge_sync<NT>();
+    const float* rin = rowml + (batch & 1) * 2 * R;
+    float* rout = rowml + ((batch + 1) & 1) * 2 * R;
+#pragma unroll 1
+    for (int gi = t; gi < R * 32; gi += NT) {
+      const int r = gi >> 5, c4 = gi & 31;
+      const float M0 = batch ? rin[2 * r] : kNegInf;
+      const float L0 = batch ? rin[2 * r + 1] : 0.f;
+      float M = M0;
+#pragma unroll 4
+      for (int p = 0; p < nbp; ++p) M = fmaxf(M, sml[(p * R + r) * 4]);
+      const float sc = (M0 == kNegInf || M == kNegInf) ? 0.f : fast_exp2(M0 - M);
+      float L = L0 * sc;
+      float4 V = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (batch) {
+        V = reinterpret_cast<const float4*>(accv)[gi];
+        V.x *= sc; V.y *= sc; V.z *= sc; V.w *= sc;
+      }
+#pragma unroll 4
+      for (int p = 0; p < nbp; ++p) {
+        const float2 ml = *reinterpret_cast<const float2*>(sml + (p * R + r) * 4);
+        const float wp = ml.x == kNegInf ? 0.f : ml.y * fast_exp2(ml.x - M);
+        const float4 o4 = reinterpret_cast<const float4*>(so + (p * R + r) * kD)[c4];
+        L += wp;
+        V.x += wp * o4.x; V.y += wp * o4.y; V.z += wp * o4.z; V.w += wp * o4.w;
+      }
+      if (last_batch) {
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        V.x *= inv; V.y *= inv; V.z *= inv; V.w *= inv;
+        store_half4(out_row(a, b, h, r) + c4 * 4, V);
+      } else {
+        reinterpret_cast<float4*>(accv)[gi] = V;
+        if (c4 == 0) { rout[2 * r] = M; rout[2 * r + 1] = L; }
+      }
+    }
+  }
+  if (t == 0) a.counters[b * a.Hkv + h] = 0;
+  merge_sync<NT>();                        // stage memory free for the next merge
+}
+
+// ---------------------------------------------------------------------------------------------
+// Warp roles: warps 0..NCW-1 consume chunks, warp NCW produces (TMA), warp NCW+1 is the
+// epilogue (merges each segment's per-warp states, writes outputs and split-unit partials,
+// announces arrivals), so the consumers never stop at a unit boundary.
 template <int NCW, int NST, int MT, bool RING>
-__global__ void __launch_bounds__((NCW + 1) * 32, MT == 1 ? 2 : 1)
+__global__ void __launch_bounds__((NCW + 2) * 32, (MT == 1 && NCW <= 4) ? 2 : 1)
 decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
   using L = Smem<NCW, NST, MT>;
-  constexpr int kNC = NCW * 32;  // consumer threads
+  // Stage st holds the CTA's chunks st, st + NST, ... and chunk j goes to consumer warp
+  // j % NCW. With NST a multiple of NCW every use of a stage goes to the same warp, which
+  // takes them in order, so it never waits on a full-barrier phase more than one ahead of the
+  // last completed one (all that a parity wait can tell apart).
+  static_assert(NST % NCW == 0, "pipeline stages must be a multiple of the consumer warps");
+  constexpr int kNC = NCW * 32;          // consumer threads
+  constexpr int kNE = (NCW + 1) * 32;    // consumers + epilogue (final merges)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -154,13 +315,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   const uint32_t bar_empty = bar_full + NST * 8;
   const uint32_t bar_qfull = bar_empty + NST * 8;
   const uint32_t bar_qempty = bar_qfull + 2 * 8;
+  const uint32_t bar_sdone = bar_qempty + 2 * 8;
+  const uint32_t bar_sfree = bar_sdone + 2 * 8;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kFlags);
-  volatile int* bcast = abort + 1;
-  float* sO = reinterpret_cast<float*>(smem + L::kScratch);
-  float* sM = sO + NCW * a.R * kD;
-  float* sL = sM + NCW * a.R;
-  float* sW = sL + NCW * a.R;
-  float* sRow = sW + NCW * a.R;
+  int* npend_s = reinterpret_cast<int*>(smem + L::kFlags) + 1;   // then 2 x (b, h, nb)
+  float* stO = reinterpret_cast<float*>(smem + L::kState);     // [2][NCW][R][128]
+  float* stM = stO + 2 * NCW * a.R * kD;                        // [2][NCW][R]
+  float* stL = stM + 2 * NCW * a.R;                             // [2][NCW][R]
+  float* ew = stL + 2 * NCW * a.R;                              // [NCW][R] epilogue weights
   int* pre = reinterpret_cast<int*>(smem + L::seq_off(a.R));
   int* slen = pre + a.num_seqs + 1;   // ctx (paged) or L (ring), clamped
   int* shw = slen + a.num_seqs;       // ring: high water
@@ -206,8 +368,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_qfull + s * 8, 1);
       mbar_init(bar_qempty + s * 8, NCW);
+      mbar_init(bar_sdone + s * 8, NCW);
+      mbar_init(bar_sfree + s * 8, 1);
     }
     *abort = 0;
+    *npend_s = 0;
     pre[0] = 0;
   }
   fence_barrier_init();
@@ -307,345 +472,380 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     return;
   }
 
-  // ===================================== consumers =============================================
-  const int w = warp;
-  const int g = lane >> 2, t4 = lane & 3;
-  int j = 0, k = 0;
-  Seg s;
-  bool has = cur.first(begin, s);
-  bool first_seg = true;
-  while (has) {
-    const int qs = k & 1;
-    const uint32_t qb = sbase + L::kQ + qs * L::kQBuf;
-    if (!mbar_wait(bar_qfull + qs * 8, (k >> 1) & 1, abort)) flag_timeout(a, abort);
-
-    const int Lc = slen[s.b];  // tokens in cache (paged ctx / ring L)
-    int lo_pos = 0, r_lo = 0;
-    if (RING) {
-      const int hw = shw[s.b];
-      lo_pos = max(a.sink, hw - a.window);
-      r_lo = a.sink + (lo_pos - a.sink) % a.window;
-      // rotate this segment's query rows in place by their own cache index
-      for (int idx = tid; idx < a.R * 64; idx += kNC) {
-        const int r = idx >> 6, d = idx & 63;
-        const int pos = Lc - a.q_len + r / a.G;
-        int jq = pos < a.sink ? pos : a.sink + (pos - lo_pos);
-        jq = min(max(jq, 0), cap - 1);
-        const uint32_t off = swz128(r, d >> 3) + (d & 7) * 2;
-        __half* px = reinterpret_cast<__half*>(smem + (qb - sbase) + off);
-        __half* py = reinterpret_cast<__half*>(smem + (qb - sbase) + L::kQHalf + off);
-        const float2 cs = __ldg(reinterpret_cast<const float2*>(a.rope) + jq * 64 + d);
-        const float x = __half2float(*px), y = __half2float(*py);
-        *px = __float2half_rn(x * cs.x - y * cs.y);
-        *py = __float2half_rn(y * cs.x + x * cs.y);
-      }
-      named_barrier_sync(1, kNC);
+  // the CTA's last segment (merged at the end by consumers and epilogue together)
+  int last_k = -1, last_b = 0, last_h = 0, last_nb = 0, last_slot = 0;
+  bool last_complete = true;
+  {
+    Seg s;
+    bool has = cur.first(begin, s);
+    int kk = 0;
+    while (has) {
+      last_k = kk;
+      last_b = s.b; last_h = s.h; last_nb = s.nb;
+      last_complete = (s.c0 == 0 && s.c1 == s.nb);
+      last_slot = 2 * blockIdx.x + (kk == 0 ? 0 : 1);
+      ++kk;
+      has = cur.next(s);
     }
+  }
 
-    // Q fragments (A operand, 16 rows x 128 dims per m-tile)
-    uint32_t qf[MT == 1 ? 8 : 1][4];
-    auto q_frag = [&](int mt, int s8, uint32_t (&f)[4]) {
-      const int i = lane >> 3;
-      const int row = mt * 16 + (i & 1) * 8 + (lane & 7);
-      const int ch = 2 * s8 + (i >> 1);
-      ldsm_x4(qb + (ch >> 3) * L::kQHalf + swz128(row, ch & 7), f[0], f[1], f[2], f[3]);
-    };
-    if (MT == 1) {
-#pragma unroll
-      for (int s8 = 0; s8 < 8; ++s8) q_frag(0, s8, qf[s8]);
-      if (RING) fence_proxy_async_smem();
+  if (warp == NCW + 1) {
+    // =================================== epilogue ============================================
+    // Merges every segment but the last as soon as the consumers hand it over, writes the
+    // output (or the partial of a split unit) and announces split units' arrivals.
+    int k = 0, npend = 0;
+    Seg s;
+    bool has = cur.first(begin, s);
+    while (has && k < last_k) {
+      const int sb = k & 1;
+      if (!mbar_wait(bar_sdone + sb * 8, (k >> 1) & 1, abort)) flag_timeout(a, abort);
+      const bool complete = (s.c0 == 0 && s.c1 == s.nb);
+      const int slot = 2 * blockIdx.x + (k == 0 ? 0 : 1);
+      merge_segment<NCW, 32>(a, stO + sb * NCW * a.R * kD, stM + sb * NCW * a.R,
+                             stL + sb * NCW * a.R, ew, s.b, s.h, complete, slot, lane);
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
+      if (lane == 0) mbar_arrive(bar_sfree + sb * 8);
+      if (!complete) {
+        // Announce the partial. The warp barrier orders the other lanes' writes before lane
+        // 0's gpu-scope fence and arrival (release); a last arrival fences again (acquire)
+        // and leaves the merge to the end of the slice, when the whole CTA can do it.
+        if (lane == 0) {
+          const int ua = pre[s.b] * a.Hkv + s.h * s.nb;
+          const int parts = (ua + s.nb - 1) / per - ua / per + 1;
+          __threadfence();
+          if (atomicAdd(a.counters + s.b * a.Hkv + s.h, 1) == parts - 1) {
+            __threadfence();
+            npend_s[1 + 3 * npend] = s.b;
+            npend_s[2 + 3 * npend] = s.h;
+            npend_s[3 + 3 * npend] = s.nb;
+            ++npend;
+          }
+        }
+      }
+      ++k;
+      has = cur.next(s);
     }
+    if (lane == 0) *npend_s = npend;
+  } else {
+    // =================================== consumers ===========================================
+    const int w = warp;
+    const int g = lane >> 2, t4 = lane & 3;
+    int j = 0, k = 0;
+    Seg s;
+    bool has = cur.first(begin, s);
+    while (has) {
+      const int qs = k & 1;
+      const uint32_t qb = sbase + L::kQ + qs * L::kQBuf;
+      if (!mbar_wait(bar_qfull + qs * 8, (k >> 1) & 1, abort)) flag_timeout(a, abort);
 
-    float m_run[MT][2], l_run[MT][2], o[MT][16][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      m_run[mt][0] = m_run[mt][1] = kNegInf;
-      l_run[mt][0] = l_run[mt][1] = 0.f;
-#pragma unroll
-      for (int nd = 0; nd < 16; ++nd) o[mt][nd][0] = o[mt][nd][1] = o[mt][nd][2] = o[mt][nd][3] = 0.f;
-    }
-    // causal limit of each of this thread's rows: query qi sees positions < Lc - q_len + qi + 1
-    int lim[MT][2];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int rh = 0; rh < 2; ++rh) {
-        const int r = mt * 16 + rh * 8 + g;
-        const int qi = r < a.R ? r / a.G : a.q_len - 1;
-        lim[mt][rh] = Lc - a.q_len + qi + 1;
+      const int Lc = slen[s.b];  // tokens in cache (paged ctx / ring L)
+      int lo_pos = 0, r_lo = 0;
+      if (RING) {
+        const int hw = shw[s.b];
+        lo_pos = max(a.sink, hw - a.window);
+        r_lo = a.sink + (lo_pos - a.sink) % a.window;
+        // rotate this segment's query rows in place by their own cache index
+        for (int idx = tid; idx < a.R * 64; idx += kNC) {
+          const int r = idx >> 6, d = idx & 63;
+          const int pos = Lc - a.q_len + r / a.G;
+          int jq = pos < a.sink ? pos : a.sink + (pos - lo_pos);
+          jq = min(max(jq, 0), cap - 1);
+          const uint32_t off = swz128(r, d >> 3) + (d & 7) * 2;
+          __half* px = reinterpret_cast<__half*>(smem + (qb - sbase) + off);
+          __half* py = reinterpret_cast<__half*>(smem + (qb - sbase) + L::kQHalf + off);
+          const float2 cs = __ldg(reinterpret_cast<const float2*>(a.rope) + jq * 64 + d);
+          const float x = __half2float(*px), y = __half2float(*py);
+          *px = __float2half_rn(x * cs.x - y * cs.y);
+          *py = __float2half_rn(y * cs.x + x * cs.y);
+        }
+        named_barrier_sync(1, kNC);   // consumers only
       }
 
-    const int nchunk = s.c1 - s.c0;
-    for (int jj = w; jj < nchunk; jj += NCW) {
-      const int gj = j + jj;
-      const int st = gj % NST;
-      if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
-      const uint32_t stK = sbase + st * kStageBytes;
-      const uint32_t stV = stK + 2 * kHalfBytes;
-      const int c = s.c0 + jj;
-
-      // positions of this thread's score columns (tokens nt*8 + 2*t4 + e) and of its K rows
-      int pcol[2][2];
-      int jk[2] = {0, 0};
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = c * kChunk + nt * 8 + 2 * t4 + e;
-          if (!RING) {
-            pcol[nt][e] = t;
-          } else {
-            int p;
-            if (t < a.sink) p = t;
-            else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; p = lo_pos + d; }
-            else p = 0x7fffffff;
-            pcol[nt][e] = p;
-          }
-        }
-        if (RING) {
-          const int t = c * kChunk + nt * 8 + g;
-          if (t < a.sink) jk[nt] = t;
-          else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; jk[nt] = a.sink + d; }
-        }
-      }
-      // whole chunk visible to every query row?
-      bool full_chunk;
-      if (!RING) full_chunk = (c + 1) * kChunk <= Lc - a.q_len + 1;
-      else full_chunk = false;
-
-      // ---- S = Q K^T ----
-      float sc[MT][2][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        uint32_t kf[8][2];
-#pragma unroll
-        for (int sp = 0; sp < 4; ++sp) {
-          const int ch = 4 * sp + (lane >> 3);
-          const int tok = nt * 8 + (lane & 7);
-          ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), kf[2 * sp][0],
-                  kf[2 * sp][1], kf[2 * sp + 1][0], kf[2 * sp + 1][1]);
-        }
-        if (RING) {
-          // rotate-half RoPE on this thread's key row (token nt*8 + g) by its cache index
-          const float4* tab = reinterpret_cast<const float4*>(a.rope) + jk[nt] * 32;
-#pragma unroll
-          for (int sp = 0; sp < 4; ++sp)
-#pragma unroll
-            for (int ri = 0; ri < 2; ++ri) {
-              const int d0 = 16 * sp + 8 * ri + 2 * t4;      // even; partner dims d0 + 64
-              const float4 cs = __ldg(tab + (d0 >> 1));
-              const float2 x = __half22float2(*reinterpret_cast<__half2*>(&kf[sp][ri]));
-              const float2 y = __half22float2(*reinterpret_cast<__half2*>(&kf[sp + 4][ri]));
-              kf[sp][ri] = pack_half2(x.x * cs.x - y.x * cs.y, x.y * cs.z - y.y * cs.w);
-              kf[sp + 4][ri] = pack_half2(y.x * cs.x + x.x * cs.y, y.y * cs.z + x.y * cs.w);
-            }
-        }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int s8 = 0; s8 < 8; ++s8) {
-            if (MT == 1) {
-              mma_16816(sc[mt][nt], qf[s8][0], qf[s8][1], qf[s8][2], qf[s8][3], kf[s8][0], kf[s8][1]);
-            } else {
-              uint32_t f[4];
-              q_frag(mt, s8, f);
-              mma_16816(sc[mt][nt], f[0], f[1], f[2], f[3], kf[s8][0], kf[s8][1]);
-            }
-          }
-      }
-
-      // ---- mask, online softmax (exp2 domain) ----
-      uint32_t pa[MT][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-        for (int rh = 0; rh < 2; ++rh) {
-          float v[4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float x = sc[mt][nt][rh * 2 + e] * a.scale_log2;
-              v[nt * 2 + e] = (full_chunk || pcol[nt][e] < lim[mt][rh]) ? x : kNegInf;
-            }
-          float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float m_new = fmaxf(m_run[mt][rh], mx);
-          const float m_use = m_new == kNegInf ? 0.f : m_new;
-          const float alpha = fast_exp2(m_run[mt][rh] - m_use);
-          m_run[mt][rh] = m_new;
-          float rs = 0.f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            v[i] = fast_exp2(v[i] - m_use);
-            rs += v[i];
-          }
-          l_run[mt][rh] = l_run[mt][rh] * alpha + rs;
-#pragma unroll
-          for (int nd = 0; nd < 16; ++nd) {
-            o[mt][nd][rh * 2] *= alpha;
-            o[mt][nd][rh * 2 + 1] *= alpha;
-          }
-          // P as the A operand: a0/a2 hold row g, a1/a3 row g+8
-          pa[mt][rh] = pack_half2(v[0], v[1]);
-          pa[mt][2 + rh] = pack_half2(v[2], v[3]);
-        }
-      }
-
-      // tokens no query may see (past the cache, or not in the ring's valid set) may hold
-      // anything, NaN included: zero their V entries so that 0 * V stays 0
-      uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-      if (!full_chunk) {
-        const int all = Lc;  // the last query's limit
-        vm0 = (pcol[0][0] < all ? 0x0000ffffu : 0u) | (pcol[0][1] < all ? 0xffff0000u : 0u);
-        vm1 = (pcol[1][0] < all ? 0x0000ffffu : 0u) | (pcol[1][1] < all ? 0xffff0000u : 0u);
-      }
-
-      // ---- O += P V ----
-#pragma unroll
-      for (int np = 0; np < 8; ++np) {
+      // Q fragments (A operand, 16 rows x 128 dims per m-tile)
+      uint32_t qf[MT == 1 ? 8 : 1][4];
+      auto q_frag = [&](int mt, int s8, uint32_t (&f)[4]) {
         const int i = lane >> 3;
-        const int tok = (i & 1) * 8 + (lane & 7);
-        const int ch = 2 * np + (i >> 1);
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(stV + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), v0, v1, v2, v3);
-        v0 &= vm0; v1 &= vm1; v2 &= vm0; v3 &= vm1;
-#pragma unroll
+        const int row = mt * 16 + (i & 1) * 8 + (lane & 7);
+        const int ch = 2 * s8 + (i >> 1);
+        ldsm_x4(qb + (ch >> 3) * L::kQHalf + swz128(row, ch & 7), f[0], f[1], f[2], f[3]);
+      };
+      if (MT == 1) {
+  #pragma unroll
+        for (int s8 = 0; s8 < 8; ++s8) q_frag(0, s8, qf[s8]);
+        if (RING) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
+      }
+
+      float m_run[MT][2], l_run[MT][2], o[MT][16][4];
+  #pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        m_run[mt][0] = m_run[mt][1] = kNegInf;
+        l_run[mt][0] = l_run[mt][1] = 0.f;
+  #pragma unroll
+        for (int nd = 0; nd < 16; ++nd) o[mt][nd][0] = o[mt][nd][1] = o[mt][nd][2] = o[mt][nd][3] = 0.f;
+      }
+      // causal limit of each of this thread's rows: query qi sees positions < Lc - q_len + qi + 1
+      int lim[MT][2];
+  #pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+  #pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          const int r = mt * 16 + rh * 8 + g;
+          const int qi = r < a.R ? r / a.G : a.q_len - 1;
+          lim[mt][rh] = Lc - a.q_len + qi + 1;
+        }
+
+      const int nchunk = s.c1 - s.c0;
+      // this warp's chunks of the segment: CTA-local index j + jj with (j + jj) % NCW == w
+      for (int jj = ((w - j) % NCW + NCW) % NCW; jj < nchunk; jj += NCW) {
+        const int gj = j + jj;
+        const int st = gj % NST;
+        if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
+        const uint32_t stK = sbase + st * kStageBytes;
+        const uint32_t stV = stK + 2 * kHalfBytes;
+        const int c = s.c0 + jj;
+
+        // positions of this thread's score columns (tokens nt*8 + 2*t4 + e) and of its K rows
+        int pcol[2][2];
+        int jk[2] = {0, 0};
+  #pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+  #pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int t = c * kChunk + nt * 8 + 2 * t4 + e;
+            if (!RING) {
+              pcol[nt][e] = t;
+            } else {
+              int p;
+              if (t < a.sink) p = t;
+              else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; p = lo_pos + d; }
+              else p = 0x7fffffff;
+              pcol[nt][e] = p;
+            }
+          }
+          if (RING) {
+            const int t = c * kChunk + nt * 8 + g;
+            if (t < a.sink) jk[nt] = t;
+            else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; jk[nt] = a.sink + d; }
+          }
+        }
+        // whole chunk visible to every query row?
+        bool full_chunk;
+        if (!RING) full_chunk = (c + 1) * kChunk <= Lc - a.q_len + 1;
+        else full_chunk = false;
+
+        // ---- S = Q K^T ----
+        // K fragments of both 8-token halves first, then two independent accumulator chains
+        // per half (even / odd k-steps) so that consecutive mma do not wait on each other.
+        uint32_t kf[2][8][2];
+  #pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+  #pragma unroll
+          for (int sp = 0; sp < 4; ++sp) {
+            const int ch = 4 * sp + (lane >> 3);
+            const int tok = nt * 8 + (lane & 7);
+            ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), kf[nt][2 * sp][0],
+                    kf[nt][2 * sp][1], kf[nt][2 * sp + 1][0], kf[nt][2 * sp + 1][1]);
+          }
+          if (RING) {
+            // rotate-half RoPE on this thread's key row (token nt*8 + g) by its cache index
+            const float4* tab = reinterpret_cast<const float4*>(a.rope) + jk[nt] * 32;
+  #pragma unroll
+            for (int sp = 0; sp < 4; ++sp)
+  #pragma unroll
+              for (int ri = 0; ri < 2; ++ri) {
+                const int d0 = 16 * sp + 8 * ri + 2 * t4;      // even; partner dims d0 + 64
+                const float4 cs = __ldg(tab + (d0 >> 1));
+                const float2 x = __half22float2(*reinterpret_cast<__half2*>(&kf[nt][sp][ri]));
+                const float2 y = __half22float2(*reinterpret_cast<__half2*>(&kf[nt][sp + 4][ri]));
+                kf[nt][sp][ri] = pack_half2(x.x * cs.x - y.x * cs.y, x.y * cs.z - y.y * cs.w);
+                kf[nt][sp + 4][ri] = pack_half2(y.x * cs.x + x.x * cs.y, y.y * cs.z + x.y * cs.w);
+              }
+          }
+        }
+        float sc[MT][2][4], sc2[MT][2][4];
+  #pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+  #pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) sc[mt][nt][i] = sc2[mt][nt][i] = 0.f;
+  #pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+  #pragma unroll
+          for (int s8 = 0; s8 < 8; ++s8) {
+            uint32_t f[4];
+            if (MT == 1) {
+              f[0] = qf[s8][0]; f[1] = qf[s8][1]; f[2] = qf[s8][2]; f[3] = qf[s8][3];
+            } else {
+              q_frag(mt, s8, f);
+            }
+  #pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+              mma_16816((s8 & 1) ? sc2[mt][nt] : sc[mt][nt], f[0], f[1], f[2], f[3],
+                        kf[nt][s8][0], kf[nt][s8][1]);
+          }
+
+        // ---- mask, online softmax (exp2 domain) ----
+        uint32_t pa[MT][4];
+        float alpha[MT][2];
+        bool rescale = false;
+  #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          mma_16816(o[mt][2 * np], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v0, v1);
-          mma_16816(o[mt][2 * np + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + st * 8);
-    }
-    if (MT != 1) {
-      if (RING) fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
-    }
-    j += nchunk;
-
-    // ---- merge the warps' states for this segment ----
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int rh = 0; rh < 2; ++rh) {
-        float lv = l_run[mt][rh];
-        lv += __shfl_xor_sync(0xffffffffu, lv, 1);
-        lv += __shfl_xor_sync(0xffffffffu, lv, 2);
-        const int r = mt * 16 + rh * 8 + g;
-        if (r < a.R) {
-          float* dst = sO + (w * a.R + r) * kD + 2 * t4;
-#pragma unroll
-          for (int nd = 0; nd < 16; ++nd)
-            *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[mt][nd][rh * 2], o[mt][nd][rh * 2 + 1]);
-          if (t4 == 0) {
-            sM[w * a.R + r] = m_run[mt][rh];
-            sL[w * a.R + r] = lv;
+  #pragma unroll
+          for (int rh = 0; rh < 2; ++rh) {
+            float v[4];
+  #pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float x = (sc[mt][nt][rh * 2 + e] + sc2[mt][nt][rh * 2 + e]) * a.scale_log2;
+                v[nt * 2 + e] = (full_chunk || pcol[nt][e] < lim[mt][rh]) ? x : kNegInf;
+              }
+            float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_old = m_run[mt][rh];
+            const float m_new = fmaxf(m_old, mx);
+            const float m_use = m_new == kNegInf ? 0.f : m_new;
+            // O and l are still exactly zero while m_old is -inf, so only a finite, grown
+            // maximum needs the accumulators rescaled
+            alpha[mt][rh] = fast_exp2(m_old - m_use);
+            rescale |= (m_old != kNegInf) && (m_new != m_old);
+            m_run[mt][rh] = m_new;
+            float rs = 0.f;
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              v[i] = fast_exp2(v[i] - m_use);
+              rs += v[i];
+            }
+            l_run[mt][rh] = l_run[mt][rh] * alpha[mt][rh] + rs;
+            // P as the A operand: a0/a2 hold row g, a1/a3 row g+8
+            pa[mt][rh] = pack_half2(v[0], v[1]);
+            pa[mt][2 + rh] = pack_half2(v[2], v[3]);
           }
         }
-      }
-    named_barrier_sync(1, kNC);
-    if (tid < a.R) {
-      float ms = kNegInf;
-      for (int ww = 0; ww < NCW; ++ww) ms = fmaxf(ms, sM[ww * a.R + tid]);
-      float ls = 0.f;
-      if (ms != kNegInf)
-        for (int ww = 0; ww < NCW; ++ww) ls += sL[ww * a.R + tid] * fast_exp2(sM[ww * a.R + tid] - ms);
-      const float inv = ls > 0.f ? 1.f / ls : 0.f;
-      for (int ww = 0; ww < NCW; ++ww)
-        sW[ww * a.R + tid] = ms == kNegInf ? 0.f : fast_exp2(sM[ww * a.R + tid] - ms) * inv;
-      sRow[2 * tid] = ms;
-      sRow[2 * tid + 1] = ls;
-    }
-    named_barrier_sync(1, kNC);
+        if (__any_sync(0xffffffffu, rescale)) {
+  #pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+  #pragma unroll
+            for (int nd = 0; nd < 16; ++nd) {
+              o[mt][nd][0] *= alpha[mt][0];
+              o[mt][nd][1] *= alpha[mt][0];
+              o[mt][nd][2] *= alpha[mt][1];
+              o[mt][nd][3] *= alpha[mt][1];
+            }
+        }
 
-    const bool complete = (s.c0 == 0 && s.c1 == s.nb);
-    const int slot = 2 * blockIdx.x + (first_seg ? 0 : 1);
-    for (int idx = tid; idx < a.R * kD; idx += kNC) {
-      const int r = idx >> 7, d = idx & (kD - 1);
-      float acc = 0.f;
-#pragma unroll
-      for (int ww = 0; ww < NCW; ++ww) acc += sO[(ww * a.R + r) * kD + d] * sW[ww * a.R + r];
-      if (complete) {
-        const int qi = r / a.G, gg = r - qi * a.G;
-        a.out[((static_cast<int64_t>(s.b) * a.q_len + qi) * a.Hq + s.h * a.G + gg) * kD + d] =
-            __float2half_rn(acc);
-      } else {
-        a.part_o[(static_cast<int64_t>(slot) * a.R + r) * kD + d] = acc;
+        // tokens no query may see (past the cache, or not in the ring's valid set) may hold
+        // anything, NaN included: zero their V entries so that 0 * V stays 0
+        uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+        if (!full_chunk) {
+          const int all = Lc;  // the last query's limit
+          vm0 = (pcol[0][0] < all ? 0x0000ffffu : 0u) | (pcol[0][1] < all ? 0xffff0000u : 0u);
+          vm1 = (pcol[1][0] < all ? 0x0000ffffu : 0u) | (pcol[1][1] < all ? 0xffff0000u : 0u);
+        }
+
+        // ---- O += P V ----
+  #pragma unroll
+        for (int np = 0; np < 8; ++np) {
+          const int i = lane >> 3;
+          const int tok = (i & 1) * 8 + (lane & 7);
+          const int ch = 2 * np + (i >> 1);
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_trans(stV + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), v0, v1, v2, v3);
+          v0 &= vm0; v1 &= vm1; v2 &= vm0; v3 &= vm1;
+  #pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            mma_16816(o[mt][2 * np], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v0, v1);
+            mma_16816(o[mt][2 * np + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + st * 8);
       }
+      if (MT != 1) {
+        if (RING) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
+      }
+      j += nchunk;
+
+      // ---- hand this warp's state for the segment to the epilogue warp ----
+      const int sb = k & 1;
+      if (k >= 2 && !mbar_wait(bar_sfree + sb * 8, ((k >> 1) - 1) & 1, abort)) flag_timeout(a, abort);
+      float* o_d = stO + sb * NCW * a.R * kD;
+  #pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+  #pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          float lv = l_run[mt][rh];
+          lv += __shfl_xor_sync(0xffffffffu, lv, 1);
+          lv += __shfl_xor_sync(0xffffffffu, lv, 2);
+          const int r = mt * 16 + rh * 8 + g;
+          if (r < a.R) {
+            float* dst = o_d + (w * a.R + r) * kD + 2 * t4;
+  #pragma unroll
+            for (int nd = 0; nd < 16; ++nd)
+              *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[mt][nd][rh * 2], o[mt][nd][rh * 2 + 1]);
+            if (t4 == 0) {
+              stM[(sb * NCW + w) * a.R + r] = m_run[mt][rh];
+              stL[(sb * NCW + w) * a.R + r] = lv;
+            }
+          }
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sdone + sb * 8);
+      ++k;
+      has = cur.next(s);
     }
-    if (!complete) {
-      if (tid < a.R) {
-        a.part_ml[(static_cast<int64_t>(slot) * a.R + tid) * 2] = sRow[2 * tid];
-        a.part_ml[(static_cast<int64_t>(slot) * a.R + tid) * 2 + 1] = sRow[2 * tid + 1];
-      }
-      __threadfence();
-      named_barrier_sync(1, kNC);
-      const int ua = pre[s.b] * a.Hkv + s.h * s.nb;  // stream index of the unit's first chunk
-      const int cf = ua / per, cl = (ua + s.nb - 1) / per;
-      if (tid == 0) {
-        const int old = atomicAdd(a.counters + s.b * a.Hkv + s.h, 1);
-        *bcast = (old == cl - cf);
-      }
-      named_barrier_sync(1, kNC);
-      if (*bcast) {
-        // last to arrive: merge the unit's partials in slice order
+  }
+
+  // ---- end of the slice: consumers and epilogue merge the last segment, then any split unit
+  // whose last partial arrived from this CTA (the producer has left)
+  if (warp != NCW && last_k >= 0) {
+    const int t = warp < NCW ? tid : tid - 32;   // dense index over consumers + epilogue
+    named_barrier_sync(2, kNE);                  // last states written, earlier segments merged
+    const int sb = last_k & 1;
+    merge_segment<NCW, kNE>(a, stO + sb * NCW * a.R * kD, stM + sb * NCW * a.R,
+                            stL + sb * NCW * a.R, ew, last_b, last_h, last_complete, last_slot, t);
+    if (!last_complete) {
+      named_barrier_sync(2, kNE);                // partial written by every thread
+      if (t == 0) {
+        const int ua = pre[last_b] * a.Hkv + last_h * last_nb;
+        const int parts = (ua + last_nb - 1) / per - ua / per + 1;
         __threadfence();
-        if (tid < a.R) {
-          float ms = kNegInf;
-          for (int cc = cf; cc <= cl; ++cc) {
-            const int sl = 2 * cc + ((cc == cf && ua != cc * per) ? 1 : 0);
-            ms = fmaxf(ms, ld_cg_f32(a.part_ml + (static_cast<int64_t>(sl) * a.R + tid) * 2));
-          }
-          float ls = 0.f;
-          if (ms != kNegInf)
-            for (int cc = cf; cc <= cl; ++cc) {
-              const int sl = 2 * cc + ((cc == cf && ua != cc * per) ? 1 : 0);
-              const float* ml = a.part_ml + (static_cast<int64_t>(sl) * a.R + tid) * 2;
-              ls += ld_cg_f32(ml + 1) * fast_exp2(ld_cg_f32(ml) - ms);
-            }
-          sRow[2 * tid] = ms;
-          sRow[2 * tid + 1] = ls > 0.f ? 1.f / ls : 0.f;
+        if (atomicAdd(a.counters + last_b * a.Hkv + last_h, 1) == parts - 1) {
+          __threadfence();
+          const int n = *npend_s;
+          npend_s[1 + 3 * n] = last_b;
+          npend_s[2 + 3 * n] = last_h;
+          npend_s[3 + 3 * n] = last_nb;
+          *npend_s = n + 1;
         }
-        named_barrier_sync(1, kNC);
-        for (int idx = tid; idx < a.R * kD; idx += kNC) {
-          const int r = idx >> 7, d = idx & (kD - 1);
-          const float ms = sRow[2 * r], inv = sRow[2 * r + 1];
-          float acc = 0.f;
-          if (ms != kNegInf)
-            for (int cc = cf; cc <= cl; ++cc) {
-              const int sl = 2 * cc + ((cc == cf && ua != cc * per) ? 1 : 0);
-              const float* ml = a.part_ml + (static_cast<int64_t>(sl) * a.R + r) * 2;
-              const float wgt = ld_cg_f32(ml + 1) * fast_exp2(ld_cg_f32(ml) - ms);
-              acc += wgt * ld_cg_f32(a.part_o + (static_cast<int64_t>(sl) * a.R + r) * kD + d);
-            }
-          const int qi = r / a.G, gg = r - qi * a.G;
-          a.out[((static_cast<int64_t>(s.b) * a.q_len + qi) * a.Hq + s.h * a.G + gg) * kD + d] =
-              __float2half_rn(acc * inv);
-        }
-        if (tid == 0) a.counters[s.b * a.Hkv + s.h] = 0;
       }
     }
-    named_barrier_sync(1, kNC);  // scratch is reused by the next segment
-    first_seg = false;
-    ++k;
-    has = cur.next(s);
+    named_barrier_sync(2, kNE);
+    const int np = *npend_s;
+    // every chunk of this CTA's slice has been consumed, so the stage memory is free
+#pragma unroll 1
+    for (int i = 0; i < np; ++i)
+      merge_unit<kNE>(a, npend_s[1 + 3 * i], npend_s[2 + 3 * i], npend_s[3 + 3 * i], pre, per,
+                      smem, NST * kStageBytes, t);
   }
 }
 
 // ---------------------------------------------------------------------------------------------
 // Host side.
-constexpr int kNCW = 4;
-constexpr int kNST = 8;
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 8
+#endif
+constexpr int kNCW = PKV_DECODE_WARPS;   // consumer warps per CTA
+constexpr int kNST = PKV_DECODE_STAGES;  // shared-memory pipeline stages per CTA
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, DecodeArgs);
 
@@ -679,7 +879,7 @@ int grid_size(const Variant& v, size_t smem, int* status) {
                            static_cast<int>(smem));
   int occ = 0;
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, (kNCW + 1) * 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, (kNCW + 2) * 32, smem);
   if (e != cudaSuccess) { *status = cuda_status(e); return 0; }
   if (occ < 1) { *status = PKV_EINVAL; return 0; }
   const int grid = sm_count() * std::min(occ, kMaxCtasPerSm);
@@ -697,7 +897,7 @@ WsLayout ws_layout(int num_seqs, int Hkv, int R) {
   WsLayout w;
   w.counters = 0;
   w.part_ml = up(static_cast<size_t>(num_seqs) * Hkv * sizeof(int));
-  w.part_o = w.part_ml + up(partials * R * 2 * sizeof(float));
+  w.part_o = w.part_ml + up(partials * R * 4 * sizeof(float));
   w.total = w.part_o + up(partials * R * kD * sizeof(float));
   return w;
 }
@@ -799,7 +999,7 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_cache, cons
   args.scale_log2 = scale * 1.4426950408889634f;
 
   void* params[4] = {&tmK, &tmV, &tmQ, &args};
-  cudaError_t e = cudaLaunchKernel(v.fn, dim3(grid), dim3((kNCW + 1) * 32), params, smem,
+  cudaError_t e = cudaLaunchKernel(v.fn, dim3(grid), dim3((kNCW + 2) * 32), params, smem,
                                    static_cast<cudaStream_t>(stream));
   return cuda_status(e);
 }

@@ -139,6 +139,14 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 __device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
 
+// 16-byte global -> shared copy that bypasses L1 (Ampere-style cp.async), and its wait.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Swizzled byte offset of 16-byte chunk `c8` (0..7) of row `row` inside a region written by a
 // TMA load with CU_TENSOR_MAP_SWIZZLE_128B (128-byte rows, region aligned to 1024 bytes).
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t c8) {

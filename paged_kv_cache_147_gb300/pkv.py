@@ -15,7 +15,8 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libpkv.so")
+# PKV_LIB selects another build of the library (e.g. a pipeline-depth variant).
+LIB_PATH = os.environ.get("PKV_LIB") or os.path.join(_HERE, "libpkv.so")
 
 # Symbols the header declares (kept in sync with include/pkv.h; the CPU tests check both).
 SYMBOLS = (
