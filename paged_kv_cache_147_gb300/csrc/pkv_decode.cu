@@ -875,8 +875,14 @@ int grid_size(const Variant& v, size_t smem, int* status) {
   auto key = std::make_tuple(dev, v.fn, smem);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
+  // The attribute is per kernel, not per launch: raise it once to the device's limit, so that
+  // a launch with a smaller size never lowers it under a later, larger one (whose grid is
+  // already cached).
+  int limit = 0;
+  e = cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess && static_cast<size_t>(limit) < smem) e = cudaErrorInvalidValue;
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
   int occ = 0;
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, (kNCW + 2) * 32, smem);
