@@ -52,7 +52,7 @@ typedef void* pkv_stream_t;
 #define PKV_OK 0
 #define PKV_EINVAL (-22)      /* bad shape, size, alignment or pointer */
 #define PKV_ERANGE (-34)      /* a host-checked index is out of range (pkv_check_*) */
-#define PKV_ENOSPC (-28)      /* workspace smaller than pkv_decode_workspace_bytes() */
+#define PKV_ENOSPC (-28)      /* workspace (or the fixed scratch array) too small for the call */
 #define PKV_ECUDA_BASE (-1000) /* PKV_ECUDA_BASE - cudaError_t of a failed CUDA call */
 
 /* ---- device error word bits ---------------------------------------------------------------- */
@@ -141,6 +141,30 @@ int pkv_paged_attn_decode(void* out, const void* q, const void* k_cache, const v
                           const int32_t* context_lens, int num_seqs, int q_len, int num_q_heads,
                           int num_kv_heads, int head_dim, int block_size, float scale,
                           void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Paged decode attention for callers that cannot allocate device memory: the same operation,
+ * arguments and result as pkv_paged_attn_decode, with the scratch (arrival counters and
+ * split-context partials) taken from a fixed array inside the library instead of a caller
+ * workspace. Meant for code that runs where it may not allocate: under a host framework that
+ * owns every device allocation (a plugin interface), in an embedded runtime with a fixed
+ * memory budget, or at a point where entering an allocator is not allowed. The pages have no
+ * counterpart of this entry point; it is an integration convenience.
+ *   - The array is 8 MiB, held by every GPU that loads the library until the process exits.
+ *     A call whose scratch would not fit (2 * SMs * 4 partial records of
+ *     (num_q_heads / num_kv_heads) * q_len rows of 528 bytes, plus 4 bytes per sequence and kv
+ *     head: for example up to 8 rows on a 152-SM GPU) returns PKV_ENOSPC and launches nothing.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree. Each call clears the arrival counters
+ *     with one cudaMemsetAsync on `stream`, then launches the decode kernel.
+ *   - The first call on a device resolves the array's device address (cudaGetSymbolAddress)
+ *     and caches it; make that first call before any stream capture.
+ *   - All calls share the one array: calls that can overlap on the GPU (different streams, or
+ *     other threads) race and corrupt each other's results. Serialise them. */
+int pkv_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, int num_blocks,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int num_seqs, int q_len,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  float scale, pkv_stream_t stream);
 
 /* RoPE table for ring attention, written to HOST memory: cos_sin[j][i][0] = cos(j * theta_i),
  * cos_sin[j][i][1] = sin(j * theta_i), theta_i = base^(-2i/head_dim), j < n_index,

@@ -1010,6 +1010,36 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_cache, cons
   return cuda_status(e);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Decode without caller-provided scratch. Some callers cannot allocate device memory at all:
+// code running under a caller that owns every device allocation (a host framework's plugin
+// interface, an embedded runtime with a fixed memory budget), or code that must not enter an
+// allocator at the point where it runs. For them the decode's scratch (arrival counters and
+// split-context partials) lives in this fixed array instead. Every GPU that loads the library
+// holds it until the process exits.
+constexpr size_t kFixedScratchBytes = size_t(8) << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kFixedScratchBytes];
+
+// Device address of g_decode_scratch on the current device. In host code the array's name is
+// only a host-side stand-in, so the address is resolved once per device (with that device
+// current) and cached.
+void* fixed_scratch(int* status) {
+  static std::mutex mu;
+  static void* ptrs[64] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { *status = cuda_status(e); return nullptr; }
+  if (dev < 0 || dev >= 64) { *status = PKV_EINVAL; return nullptr; }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) { *status = cuda_status(e); return nullptr; }
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -1054,6 +1084,32 @@ int pkv_ring_attn_decode(void* out, const void* q, const void* k_cache, const vo
                        max_blocks_per_seq, nullptr, logical_len, high_water, num_seqs, q_len,
                        num_q_heads, num_kv_heads, head_dim, block_size, sink, window,
                        rope_cos_sin, scale, workspace, workspace_bytes, stream);
+}
+
+int pkv_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, int num_blocks,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int num_seqs, int q_len,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  float scale, pkv_stream_t stream) {
+  if (num_seqs > 0 && q_len >= 1 && num_q_heads >= 1 && num_kv_heads >= 1 &&
+      num_q_heads % num_kv_heads == 0 && head_dim == kD) {
+    const int R = num_q_heads / num_kv_heads * q_len;
+    if (sm_count() == 0) return cuda_status(cudaGetLastError());
+    const WsLayout ws = ws_layout(num_seqs, num_kv_heads, R);
+    if (ws.total > kFixedScratchBytes) return PKV_ENOSPC;
+    int status = PKV_OK;
+    void* scratch = fixed_scratch(&status);
+    if (!scratch) return status;
+    // the array keeps the previous call's contents; the arrival counters must start at zero
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, ws.part_ml, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+    return pkv_paged_attn_decode(out, q, k_cache, v_cache, num_blocks, block_tables,
+                                 max_blocks_per_seq, context_lens, num_seqs, q_len, num_q_heads,
+                                 num_kv_heads, head_dim, block_size, scale, scratch,
+                                 kFixedScratchBytes, stream);
+  }
+  return num_seqs == 0 ? PKV_OK : PKV_EINVAL;
 }
 
 }  // extern "C"

@@ -23,7 +23,7 @@ SYMBOLS = (
     "pkv_version", "pkv_device_error", "pkv_slot_mapping", "pkv_ring_slot_mapping",
     "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes", "pkv_workspace_init",
     "pkv_paged_attn_decode", "pkv_rope_table", "pkv_ring_attn_decode", "pkv_check_tables",
-    "pkv_check_slots",
+    "pkv_check_slots", "pkv_paged_attn_decode_noalloc",
 )
 
 OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
                                            i32, i32, i32, i32, P, f32, P, sz, P]),
             "pkv_check_tables": (i32, [P, P, i32, i32, i32, i32, P]),
             "pkv_check_slots": (i32, [P, i32, i32, i32, P]),
+            "pkv_paged_attn_decode_noalloc": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32,
+                                                    i32, i32, i32, f32, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -175,6 +177,19 @@ def paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, scal
         _p(out), _p(q), _p(k_cache), _p(v_cache), nb, _p(block_tables), block_tables.shape[1],
         _p(context_lens), B, q_len, hq, hkv, d, bs, float(scale), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def paged_attn_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                              stream=None):
+    """paged_attn_decode for callers that cannot allocate device memory: the library's fixed
+    8 MiB scratch array replaces the workspace. Calls sharing it must not overlap on the GPU;
+    the first call on a device must come before any stream capture."""
+    B, q_len, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_paged_attn_decode_noalloc", load().pkv_paged_attn_decode_noalloc(
+        _p(out), _p(q), _p(k_cache), _p(v_cache), nb, _p(block_tables), block_tables.shape[1],
+        _p(context_lens), B, q_len, hq, hkv, d, bs, float(scale), _stream(stream)))
     return out
 
 
