@@ -259,6 +259,18 @@ def test_block_permutation_and_sharing_are_bit_identical():
     assert torch.equal(base, _gpu_decode(k, v, tables, lens, q, scale))
 
 
+def test_launch_sizes_can_shrink_and_grow_again():
+    """A decode with a smaller shared-memory footprint (fewer sequences) between two larger
+    ones must not break the larger launch (the kernel attribute is per kernel, not per call)."""
+    scale = 0.1
+    big = _small([100] * 600, seed=31, poison=False)
+    small = _small([100, 7], seed=32, poison=False)
+    for k, v, tables, lens, q in (big, small, big):
+        out = _gpu_decode(k, v, tables, lens, q, scale)
+        ref = oracle.paged_attention(q, k, v, tables, lens, 16, scale)
+        assert_attn_close(out, ref, f"B={len(lens)}")
+
+
 def test_single_token_context_is_v_exactly():
     k, v, tables, lens, q = _small([1, 1, 1], poison=True)
     out = _gpu_decode(k, v, tables, lens, q, 0.3)
