@@ -153,15 +153,15 @@ class Step:
         self.out = torch.empty_like(self.q)
         self.slots = torch.empty(seq.shape[0], dtype=torch.int64, device=dev)
         self.ws = pkv.make_workspace(w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, dev)
-        self.launches_per_step = 1 + 2 * Lr
+        self.launches_per_step = Lr
 
     def run(self):
+        """One decode step: per layer, the fused call appends the new K/V rows at the slots the
+        block table gives (slot mapping + append) and runs paged decode attention."""
         p, w = self.pkv, self.w
-        p.slot_mapping(self.seq, self.pos, self.bt, w.block_size, out=self.slots)
         for l in range(w.num_layers):
-            p.kv_append(self.kn[l], self.vn[l], self.slots, self.k[l], self.v[l])
-            p.paged_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.cl,
-                                w.scale, self.ws)
+            p.paged_attn_decode_append(self.out[l], self.q[l], self.kn[l], self.vn[l], self.k[l],
+                                       self.v[l], self.bt, self.cl, w.scale, self.ws)
 
     def run_decode_only(self):
         p, w = self.pkv, self.w
@@ -287,8 +287,8 @@ def run_ours(args, w, rank, local_rank, world_size):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t_max / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": describe(w) | {"graph": f"CUDA graph: slot mapping + {w.num_layers} x "
-                                          "(kv_append, paged_attn_decode)",
+        "config": describe(w) | {"graph": f"CUDA graph: {w.num_layers} x paged_attn_decode_append "
+                                          "(slot mapping + KV append + decode, one launch)",
                                  "parallelism": f"replicas x{world_size}"},
         "decode_tokens_per_s": round(w.num_seqs * w.q_len * args.steps * world_size / t_max, 1),
         "pct_of_nominal_8tbs": round(100 * value / world_size / NOMINAL_HBM_GBS, 2),

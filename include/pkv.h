@@ -142,6 +142,23 @@ int pkv_paged_attn_decode(void* out, const void* q, const void* k_cache, const v
                           int num_kv_heads, int head_dim, int block_size, float scale,
                           void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
+/* Decode step with the KV append fused in: for every sequence b and new token i < q_len, the
+ * token at position p = context_lens[b] - q_len + i (p >= 0) has its K/V rows k_new, v_new
+ * [(b * q_len + i)][kh][:] written to the slot the block table maps p to (the slot of
+ * pkv_slot_mapping), exactly as pkv_kv_append would; the attention of pkv_paged_attn_decode then
+ * runs over the cache including them ([VLLM] on-demand paging + PagedAttention kernel
+ * paragraph). One launch instead of slot mapping + append + decode; the new rows are read once
+ * and used both for the pool and for this step's attention. k_new, v_new (device): fp16
+ * [num_seqs * q_len][num_kv_heads][head_dim]; other arguments as for pkv_paged_attn_decode. The
+ * slots written must not be shared with another sequence (copy-on-write first). */
+int pkv_paged_attn_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, int num_blocks,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int num_seqs, int q_len,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                 float scale, void* workspace, size_t workspace_bytes,
+                                 pkv_stream_t stream);
+
 /* Paged decode attention for callers that cannot allocate device memory: the same operation,
  * arguments and result as pkv_paged_attn_decode, with the scratch (arrival counters and
  * split-context partials) taken from a fixed array inside the library instead of a caller

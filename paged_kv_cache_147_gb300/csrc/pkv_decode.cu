@@ -65,6 +65,11 @@ struct DecodeArgs {
   int block_size, bs_shift;     // bs_shift = log2(block_size / 16)
   int sink, window;
   float scale_log2;             // scale * log2(e)
+  // fused append: this step's new K/V rows [B*q_len][Hkv][128] and the layer's pools
+  const __half* k_new;
+  const __half* v_new;
+  __half* k_pool;
+  __half* v_pool;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -83,14 +88,19 @@ struct Smem {
   // full[NST], empty[NST], qfull[2], qempty[2], sdone[2], sfree[2]
   static constexpr int kBars = kQ + 2 * kQBuf;
   static constexpr int kFlags = kBars + (2 * NST + 8) * 8;  // abort, pending count + units
-  static constexpr int kState = kFlags + 64;
+  static constexpr int kSrow = kFlags + 64;             // TMA row of each stage's chunk
+  static constexpr int kState = kSrow + ((NST * 4 + 15) & ~15);
   // segment states handed from the consumer warps to the epilogue warp, double-buffered:
   // o [2][NCW][R][128], m [2][NCW][R], l [2][NCW][R]; then the epilogue's weights [NCW][R]
   __host__ __device__ static int state_floats(int R) { return 2 * NCW * R * (kD + 2) + NCW * R; }
   __host__ __device__ static int seq_off(int R) { return kState + state_floats(R) * 4; }
-  // per sequence: prefix (B+1 ints), length, high water
-  __host__ static size_t bytes(int R, int B) {
-    return 1024 + static_cast<size_t>(seq_off(R)) + static_cast<size_t>(3 * B + 1) * 4;
+  // per sequence: prefix (B+1 ints), length, high water; then (fused append) the new K/V
+  // rows of the current segment, double-buffered with its queries: [2][q_len][K|V][256 B]
+  __host__ __device__ static int newkv_off(int R, int B) {
+    return (seq_off(R) + (3 * B + 1) * 4 + 127) & ~127;
+  }
+  __host__ static size_t bytes(int R, int B, int newkv_bytes) {
+    return 1024 + static_cast<size_t>(newkv_off(R, B)) + static_cast<size_t>(newkv_bytes);
   }
 };
 
@@ -295,7 +305,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
 // Warp roles: warps 0..NCW-1 consume chunks, warp NCW produces (TMA), warp NCW+1 is the
 // epilogue (merges each segment's per-warp states, writes outputs and split-unit partials,
 // announces arrivals), so the consumers never stop at a unit boundary.
-template <int NCW, int NST, int MT, bool RING>
+template <int NCW, int NST, int MT, bool RING, bool APPEND>
 __global__ void __launch_bounds__((NCW + 2) * 32, (MT == 1 && NCW <= 4) ? 2 : 1)
 decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
@@ -305,6 +315,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   // takes them in order, so it never waits on a full-barrier phase more than one ahead of the
   // last completed one (all that a parity wait can tell apart).
   static_assert(NST % NCW == 0, "pipeline stages must be a multiple of the consumer warps");
+  static_assert(!(RING && APPEND), "the ring variant appends through its own slot mapping");
+  // the queries' buffer stays in use for the whole segment when its fragments are not kept in
+  // registers, or when it also holds the segment's new K/V rows
+  constexpr bool kHoldQ = MT != 1 || APPEND;
   constexpr int kNC = NCW * 32;          // consumer threads
   constexpr int kNE = (NCW + 1) * 32;    // consumers + epilogue (final merges)
   extern __shared__ uint8_t smem_raw[];
@@ -318,6 +332,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   const uint32_t bar_sdone = bar_qempty + 2 * 8;
   const uint32_t bar_sfree = bar_sdone + 2 * 8;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kFlags);
+  int* srow_s = reinterpret_cast<int*>(smem + L::kSrow);
   int* npend_s = reinterpret_cast<int*>(smem + L::kFlags) + 1;   // then 2 x (b, h, nb)
   float* stO = reinterpret_cast<float*>(smem + L::kState);     // [2][NCW][R][128]
   float* stM = stO + 2 * NCW * a.R * kD;                        // [2][NCW][R]
@@ -425,10 +440,18 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const int qs = k & 1;
         if (k >= 2 && !mbar_wait(bar_qempty + qs * 8, ((k >> 1) - 1) & 1, abort))
           flag_timeout(a, abort);
-        mbar_arrive_expect_tx(bar_qfull + qs * 8, a.R * 256);
+        mbar_arrive_expect_tx(bar_qfull + qs * 8, a.R * 256 + (APPEND ? a.q_len * 512 : 0));
         const uint32_t qdst = sbase + L::kQ + qs * L::kQBuf;
         tma_load_3d(qdst, &tmQ, 0, s.h * a.G, s.b * a.q_len, bar_qfull + qs * 8);
         tma_load_3d(qdst + L::kQHalf, &tmQ, 64, s.h * a.G, s.b * a.q_len, bar_qfull + qs * 8);
+        if (APPEND) {
+          const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
+          for (int i = 0; i < a.q_len; ++i) {
+            const int64_t row = (static_cast<int64_t>(s.b) * a.q_len + i) * a.Hkv + s.h;
+            bulk_load(nkv + i * 512, a.k_new + row * kD, 256, bar_qfull + qs * 8);
+            bulk_load(nkv + i * 512 + 256, a.v_new + row * kD, 256, bar_qfull + qs * 8);
+          }
+        }
       }
       const int32_t* bt = a.block_tables + static_cast<int64_t>(s.b) * a.max_blocks;
       for (int cb = s.c0; cb < s.c1; cb += 32) {
@@ -449,6 +472,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (j >= NST && !mbar_wait(bar_empty + st * 8, ((j / NST) - 1) & 1, abort))
               flag_timeout(a, abort);
             const uint32_t fb = bar_full + st * 8;
+            if (APPEND) srow_s[st] = r;   // published to the consumer by the barrier below
             mbar_arrive_expect_tx(fb, kStageBytes);
             const uint32_t dst = sbase + st * kStageBytes;
             tma_load_2d(dst, &tmK, 0, r, fb);
@@ -570,11 +594,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         ldsm_x4(qb + (ch >> 3) * L::kQHalf + swz128(row, ch & 7), f[0], f[1], f[2], f[3]);
       };
       if (MT == 1) {
-  #pragma unroll
+#pragma unroll
         for (int s8 = 0; s8 < 8; ++s8) q_frag(0, s8, qf[s8]);
-        if (RING) fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
+        if (!kHoldQ) {
+          if (RING) fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
+        }
       }
 
       float m_run[MT][2], l_run[MT][2], o[MT][16][4];
@@ -634,6 +660,31 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         bool full_chunk;
         if (!RING) full_chunk = (c + 1) * kChunk <= Lc - a.q_len + 1;
         else full_chunk = false;
+
+        // ---- fused append: this chunk holds some of the step's new tokens (the last q_len
+        // positions of the sequence). Their K/V rows, loaded with the segment's queries, replace
+        // the stale slots in the landed tile and are written to the pool (the chunk's TMA row
+        // plus the token's offset: the slot the table maps that position to). ----
+        bool patched = false;
+        if (APPEND && (c + 1) * kChunk > Lc - a.q_len) {
+          const int first_new = Lc - a.q_len;
+          const int srow = srow_s[st];
+          const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
+          const int which = lane >> 4, ch = lane & 15;   // lanes 0-15: K, 16-31: V
+          for (int i = 0; i < a.q_len; ++i) {
+            const int pos = first_new + i;
+            if (pos < c * kChunk || pos >= (c + 1) * kChunk || pos < 0) continue;
+            const int tok = pos - c * kChunk;
+            const uint4 val = ld_shared_v4(nkv + i * 512 + which * 256 + ch * 16);
+            st_shared_v4((which ? stV : stK) + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), val);
+            if (srow >= 0) {
+              __half* pool = which ? a.v_pool : a.k_pool;
+              *reinterpret_cast<uint4*>(pool + (static_cast<int64_t>(srow) + tok) * kD + ch * 8) = val;
+            }
+          }
+          __syncwarp();
+          patched = true;
+        }
 
         // ---- S = Q K^T ----
         // K fragments of both 8-token halves first, then two independent accumulator chains
@@ -762,10 +813,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             mma_16816(o[mt][2 * np + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
           }
         }
+        // a patched tile was written through the generic proxy; order that before the next
+        // TMA (async proxy) write into this stage
+        if (APPEND && patched) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + st * 8);
       }
-      if (MT != 1) {
+      if (kHoldQ) {
         if (RING) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
@@ -855,13 +909,15 @@ struct Variant {
   bool ring;
 };
 
-template <int MT, bool RING>
+template <int MT, bool RING, bool APPEND>
 Variant variant() {
-  return Variant{reinterpret_cast<const void*>(&decode_kernel<kNCW, kNST, MT, RING>), MT, RING};
+  return Variant{reinterpret_cast<const void*>(&decode_kernel<kNCW, kNST, MT, RING, APPEND>), MT,
+                 RING};
 }
 
-size_t smem_bytes(int mt, int R, int B) {
-  return mt == 1 ? Smem<kNCW, kNST, 1>::bytes(R, B) : Smem<kNCW, kNST, 2>::bytes(R, B);
+size_t smem_bytes(int mt, int R, int B, int newkv_bytes) {
+  return mt == 1 ? Smem<kNCW, kNST, 1>::bytes(R, B, newkv_bytes)
+                 : Smem<kNCW, kNST, 2>::bytes(R, B, newkv_bytes);
 }
 
 // Persistent grid for a variant: SM count x resident CTAs (capped), cached per device/size.
@@ -919,7 +975,8 @@ int encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
   return r == CUDA_SUCCESS ? PKV_OK : PKV_EINVAL;
 }
 
-int launch_decode(bool ring, void* out, const void* q, const void* k_cache, const void* v_cache,
+int launch_decode(bool ring, void* out, const void* q, const void* k_new, const void* v_new,
+                  const void* k_cache, const void* v_cache,
                   int num_blocks, const int32_t* block_tables, int max_blocks,
                   const int32_t* context_lens, const int64_t* logical_len,
                   const int64_t* high_water, int num_seqs, int q_len, int Hq, int Hkv,
@@ -937,6 +994,8 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_cache, cons
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return PKV_EINVAL;
+  const bool append = k_new != nullptr;
+  if (append && (ring || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
   if (ring) {
     if (!logical_len || !high_water || !rope || sink < 0 || window < 1) return PKV_EINVAL;
     if ((sink + window + block_size - 1) / block_size > max_blocks) return PKV_EINVAL;
@@ -953,9 +1012,10 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_cache, cons
   if (workspace_bytes < ws.total) return PKV_ENOSPC;
 
   const int mt = R <= 16 ? 1 : 2;
-  Variant v = ring ? (mt == 1 ? variant<1, true>() : variant<2, true>())
-                   : (mt == 1 ? variant<1, false>() : variant<2, false>());
-  const size_t smem = smem_bytes(mt, R, num_seqs);
+  Variant v = ring     ? (mt == 1 ? variant<1, true, false>() : variant<2, true, false>())
+              : append ? (mt == 1 ? variant<1, false, true>() : variant<2, false, true>())
+                       : (mt == 1 ? variant<1, false, false>() : variant<2, false, false>());
+  const size_t smem = smem_bytes(mt, R, num_seqs, append ? 2 * q_len * 512 : 0);
   if (smem > 227 * 1024) return PKV_EINVAL;
   int status = PKV_OK;
   const int grid = grid_size(v, smem, &status);
@@ -1003,6 +1063,10 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_cache, cons
   args.sink = sink;
   args.window = window;
   args.scale_log2 = scale * 1.4426950408889634f;
+  args.k_new = static_cast<const __half*>(k_new);
+  args.v_new = static_cast<const __half*>(v_new);
+  args.k_pool = static_cast<__half*>(const_cast<void*>(k_cache));
+  args.v_pool = static_cast<__half*>(const_cast<void*>(v_cache));
 
   void* params[4] = {&tmK, &tmV, &tmQ, &args};
   cudaError_t e = cudaLaunchKernel(v.fn, dim3(grid), dim3((kNCW + 2) * 32), params, smem,
@@ -1067,10 +1131,24 @@ int pkv_paged_attn_decode(void* out, const void* q, const void* k_cache, const v
                           const int32_t* context_lens, int num_seqs, int q_len, int num_q_heads,
                           int num_kv_heads, int head_dim, int block_size, float scale,
                           void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
-  return launch_decode(false, out, q, k_cache, v_cache, num_blocks, block_tables,
+  return launch_decode(false, out, q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables,
                        max_blocks_per_seq, context_lens, nullptr, nullptr, num_seqs, q_len,
                        num_q_heads, num_kv_heads, head_dim, block_size, 0, 1, nullptr, scale,
                        workspace, workspace_bytes, stream);
+}
+
+int pkv_paged_attn_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, int num_blocks,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int num_seqs, int q_len,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                 float scale, void* workspace, size_t workspace_bytes,
+                                 pkv_stream_t stream) {
+  if (num_seqs > 0 && (!k_new || !v_new)) return PKV_EINVAL;
+  return launch_decode(false, out, q, num_seqs > 0 ? k_new : nullptr, v_new, k_cache, v_cache,
+                       num_blocks, block_tables, max_blocks_per_seq, context_lens, nullptr,
+                       nullptr, num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                       0, 1, nullptr, scale, workspace, workspace_bytes, stream);
 }
 
 int pkv_ring_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -1080,7 +1158,7 @@ int pkv_ring_attn_decode(void* out, const void* q, const void* k_cache, const vo
                          int block_size, int sink, int window, const float* rope_cos_sin,
                          float scale, void* workspace, size_t workspace_bytes,
                          pkv_stream_t stream) {
-  return launch_decode(true, out, q, k_cache, v_cache, num_blocks, block_tables,
+  return launch_decode(true, out, q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables,
                        max_blocks_per_seq, nullptr, logical_len, high_water, num_seqs, q_len,
                        num_q_heads, num_kv_heads, head_dim, block_size, sink, window,
                        rope_cos_sin, scale, workspace, workspace_bytes, stream);

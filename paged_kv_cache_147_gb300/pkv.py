@@ -23,7 +23,7 @@ SYMBOLS = (
     "pkv_version", "pkv_device_error", "pkv_slot_mapping", "pkv_ring_slot_mapping",
     "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes", "pkv_workspace_init",
     "pkv_paged_attn_decode", "pkv_rope_table", "pkv_ring_attn_decode", "pkv_check_tables",
-    "pkv_check_slots", "pkv_paged_attn_decode_noalloc",
+    "pkv_check_slots", "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_decode_append",
 )
 
 OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
@@ -76,6 +76,8 @@ def load() -> ctypes.CDLL:
             "pkv_check_slots": (i32, [P, i32, i32, i32, P]),
             "pkv_paged_attn_decode_noalloc": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32,
                                                     i32, i32, i32, f32, P]),
+            "pkv_paged_attn_decode_append": (i32, [P, P, P, P, P, P, i32, P, i32, P, i32, i32,
+                                                   i32, i32, i32, i32, f32, P, sz, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -177,6 +179,19 @@ def paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, scal
         _p(out), _p(q), _p(k_cache), _p(v_cache), nb, _p(block_tables), block_tables.shape[1],
         _p(context_lens), B, q_len, hq, hkv, d, bs, float(scale), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def paged_attn_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                             scale, workspace, stream=None):
+    """Decode step with the KV append fused in: k_new, v_new [B*q_len, Hkv, D] go to the slots of
+    positions context_lens[b] - q_len + i, then attention runs over the cache including them."""
+    B, q_len, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_paged_attn_decode_append", load().pkv_paged_attn_decode_append(
+        _p(out), _p(q), _p(k_new), _p(v_new), _p(k_cache), _p(v_cache), nb, _p(block_tables),
+        block_tables.shape[1], _p(context_lens), B, q_len, hq, hkv, d, bs, float(scale),
+        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 
 

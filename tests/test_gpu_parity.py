@@ -24,21 +24,27 @@ def _dev(a, dtype):
     return torch.as_tensor(np.ascontiguousarray(a), dtype=dtype, device=DEV)
 
 
-def _run_decode_layer(w, k_l, v_l, bt_d, cl_d, slots_d, q, kn, vn, ws):
-    pkv.kv_append(kn, vn, slots_d, k_l, v_l)
+def _run_decode_layer(w, k_l, v_l, bt_d, cl_d, slots_d, q, kn, vn, ws, fused=False):
     out = torch.empty_like(q)
-    pkv.paged_attn_decode(out, q, k_l, v_l, bt_d, cl_d, w.scale, ws)
+    if fused:
+        pkv.paged_attn_decode_append(out, q, kn, vn, k_l, v_l, bt_d, cl_d, w.scale, ws)
+    else:
+        pkv.kv_append(kn, vn, slots_d, k_l, v_l)
+        pkv.paged_attn_decode(out, q, k_l, v_l, bt_d, cl_d, w.scale, ws)
     return out
 
 
-def _check_layer(w, layer, k_all, v_all, bt_d, cl_d, slots_d, orc_slots, ws, seq_mask=None):
-    """Append + decode one layer on the GPU; the oracle redoes the append on a host copy of
-    the pre-append pool and attends over its own copy."""
+def _check_layer(w, layer, k_all, v_all, bt_d, cl_d, slots_d, orc_slots, ws, seq_mask=None,
+                 fused=False):
+    """Append + decode one layer on the GPU (separate calls, or the fused entry point); the
+    oracle redoes the append on a host copy of the pre-append pool and attends over its own
+    copy."""
     k_host = f16_host(k_all[layer]).copy()
     v_host = f16_host(v_all[layer]).copy()
     q = w.query(layer, DEV)
     kn, vn = w.new_kv(layer, DEV)
-    out = _run_decode_layer(w, k_all[layer], v_all[layer], bt_d, cl_d, slots_d, q, kn, vn, ws)
+    out = _run_decode_layer(w, k_all[layer], v_all[layer], bt_d, cl_d, slots_d, q, kn, vn, ws,
+                            fused)
     torch.cuda.synchronize()
     oracle.kv_append(f16_host(kn), f16_host(vn), orc_slots, k_host, v_host, w.block_size)
     assert np.array_equal(u16(k_all[layer]), k_host.view(np.uint16)), f"K pool layer {layer}"
@@ -94,6 +100,51 @@ def test_llama70b_sampled_layers(make):
     state = _setup(w)
     for layer in (0, 1, 40, 79):
         _check_layer(w, layer, *state)
+
+
+@pytest.mark.parametrize("make,layers", [(workloads.tiny, (0,)),
+                                         (workloads.edge_1p1b, tuple(range(24))),
+                                         (workloads.llama70b_mixed, (0, 79))])
+def test_fused_append_decode(make, layers):
+    w = make()
+    state = _setup(w)
+    for layer in layers:
+        _check_layer(w, layer, *state, fused=True)
+
+
+@pytest.mark.parametrize("q_len,lens", [(2, [33, 16, 2, 100]), (4, [64, 5, 31, 4]), (3, [1000, 47])])
+def test_fused_append_multi_token(q_len, lens):
+    """Several new tokens per sequence, straddling chunk and block boundaries."""
+    rng = np.random.default_rng(q_len)
+    lens = np.asarray(lens, dtype=np.int32)
+    bs, hkv, hq = 16, 2, 8
+    nblk = [(int(x) + bs - 1) // bs for x in lens]
+    nb = sum(nblk) + 2
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = np.full((len(lens), max(nblk)), -1, np.int32)
+    cur = 0
+    for b, n in enumerate(nblk):
+        tables[b, :n] = perm[cur:cur + n]
+        cur += n
+    k = rng.standard_normal((nb, hkv, bs, 128)).astype(np.float16)
+    v = rng.standard_normal((nb, hkv, bs, 128)).astype(np.float16)
+    q = rng.standard_normal((len(lens), q_len, hq, 128)).astype(np.float16)
+    kn = rng.standard_normal((len(lens) * q_len, hkv, 128)).astype(np.float16)
+    vn = rng.standard_normal((len(lens) * q_len, hkv, 128)).astype(np.float16)
+    kd, vd = torch.from_numpy(k).to(DEV), torch.from_numpy(v).to(DEV)
+    out = torch.empty((len(lens), q_len, hq, 128), dtype=torch.float16, device=DEV)
+    ws = pkv.make_workspace(len(lens), q_len, hq, hkv)
+    pkv.paged_attn_decode_append(out, torch.from_numpy(q).to(DEV), torch.from_numpy(kn).to(DEV),
+                                 torch.from_numpy(vn).to(DEV), kd, vd, _dev(tables, torch.int32),
+                                 _dev(lens, torch.int32), 0.09, ws)
+    torch.cuda.synchronize()
+    seq = np.repeat(np.arange(len(lens), dtype=np.int32), q_len)
+    pos = (lens[:, None] - q_len + np.arange(q_len)[None, :]).reshape(-1).astype(np.int64)
+    slots = oracle.slot_mapping(seq, pos, tables, bs)
+    oracle.kv_append(kn, vn, slots, k, v, bs)
+    assert np.array_equal(u16(kd), k.view(np.uint16)) and np.array_equal(u16(vd), v.view(np.uint16))
+    ref = oracle.paged_attention(q, k, v, tables, lens, bs, 0.09)
+    assert_attn_close(out, ref, f"fused q_len={q_len}")
 
 
 def test_prefix_fork_copy_on_write():
