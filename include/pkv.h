@@ -150,7 +150,13 @@ int pkv_paged_attn_decode(void* out, const void* q, const void* k_cache, const v
  * paragraph). One launch instead of slot mapping + append + decode; the new rows are read once
  * and used both for the pool and for this step's attention. k_new, v_new (device): fp16
  * [num_seqs * q_len][num_kv_heads][head_dim]; other arguments as for pkv_paged_attn_decode. The
- * slots written must not be shared with another sequence (copy-on-write first). */
+ * slots written must not be shared with another sequence (copy-on-write first).
+ * Launch overlap: this call is launched with programmatic dependent launch, so it may start
+ * while the kernel before it on the stream is still finishing. Before that kernel completes it
+ * reads only the K/V pools, block_tables and context_lens; q, k_new, v_new, out and the workspace
+ * are touched after. Those three inputs must therefore not be written by the immediately
+ * preceding kernel (in particular not by a preceding pkv_paged_attn_decode_append on the same
+ * pools). The library's other kernels never let the next kernel start early. */
 int pkv_paged_attn_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
                                  void* k_cache, void* v_cache, int num_blocks,
                                  const int32_t* block_tables, int max_blocks_per_seq,

@@ -416,56 +416,84 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   const int begin = blockIdx.x * per;
   const Cursor cur{pre, B, a.Hkv, min(total, begin + per)};
 
-  // sequences without any chunk get zeros (their units are in no CTA's slice)
-  for (int b = blockIdx.x; b < B; b += gridDim.x) {
-    if (pre[b + 1] != pre[b]) continue;
-    const int n = a.q_len * a.Hq * kD;
-    for (int i = tid; i < n; i += blockDim.x)
-      a.out[static_cast<int64_t>(b) * n + i] = __float2half_rn(0.f);
-  }
+  // let the next kernel on the stream launch as soon as SM resources free up (its own
+  // dependency wait keeps it from reading anything this kernel writes)
+  if (tid == 0) griddep_launch_dependents();
 
   if (warp == NCW) {
     // =================================== producer ============================================
+    const int chunk_mask = (1 << a.bs_shift) - 1;
+    int j = 0, k = 0;
+    Seg s;
+    bool has = cur.first(begin, s);
+    // block-table entries of the next 32 chunks, loaded one group ahead of their use
+    auto load_ids = [&](const Seg& sg, int cb) -> int32_t {
+      const int cc = cb + lane;
+      return cc < sg.c1 ? __ldg(a.block_tables + static_cast<int64_t>(sg.b) * a.max_blocks +
+                                (cc >> a.bs_shift))
+                        : -1;
+    };
+    int32_t ids = has ? load_ids(s, s.c0) : -1;
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       prefetch_tensormap(&tmQ);
     }
-    const int chunk_mask = (1 << a.bs_shift) - 1;
-    int j = 0, k = 0;
-    Seg s;
-    bool has = cur.first(begin, s);
-    while (has) {
-      if (lane == 0) {
-        const int qs = k & 1;
-        if (k >= 2 && !mbar_wait(bar_qempty + qs * 8, ((k >> 1) - 1) & 1, abort))
-          flag_timeout(a, abort);
-        mbar_arrive_expect_tx(bar_qfull + qs * 8, a.R * 256 + (APPEND ? a.q_len * 512 : 0));
-        const uint32_t qdst = sbase + L::kQ + qs * L::kQBuf;
-        tma_load_3d(qdst, &tmQ, 0, s.h * a.G, s.b * a.q_len, bar_qfull + qs * 8);
-        tma_load_3d(qdst + L::kQHalf, &tmQ, 64, s.h * a.G, s.b * a.q_len, bar_qfull + qs * 8);
-        if (APPEND) {
-          const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
-          for (int i = 0; i < a.q_len; ++i) {
-            const int64_t row = (static_cast<int64_t>(s.b) * a.q_len + i) * a.Hkv + s.h;
-            bulk_load(nkv + i * 512, a.k_new + row * kD, 256, bar_qfull + qs * 8);
-            bulk_load(nkv + i * 512 + 256, a.v_new + row * kD, 256, bar_qfull + qs * 8);
-          }
+    // The fused-append variant may be launched before the preceding kernel on the stream has
+    // finished (programmatic dependent launch). Its K/V pool, block tables and context lengths
+    // are not written by that kernel, so the first NST chunks are requested right away; the
+    // queries, the new K/V rows, the output and the workspace are touched only after
+    // griddepcontrol.wait. The other variants wait before their first query load (a no-op,
+    // as they are never launched early).
+    const bool early_kv = APPEND;
+    bool waited = false;
+    const Seg first_seg = s;
+    auto issue_q = [&](const Seg& sg, int kk) {
+      if (lane != 0) return;
+      const int qs = kk & 1;
+      if (kk >= 2 && !mbar_wait(bar_qempty + qs * 8, ((kk >> 1) - 1) & 1, abort))
+        flag_timeout(a, abort);
+      mbar_arrive_expect_tx(bar_qfull + qs * 8, a.R * 256 + (APPEND ? a.q_len * 512 : 0));
+      const uint32_t qdst = sbase + L::kQ + qs * L::kQBuf;
+      tma_load_3d(qdst, &tmQ, 0, sg.h * a.G, sg.b * a.q_len, bar_qfull + qs * 8);
+      tma_load_3d(qdst + L::kQHalf, &tmQ, 64, sg.h * a.G, sg.b * a.q_len, bar_qfull + qs * 8);
+      if (APPEND) {
+        const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
+        for (int i = 0; i < a.q_len; ++i) {
+          const int64_t row = (static_cast<int64_t>(sg.b) * a.q_len + i) * a.Hkv + sg.h;
+          bulk_load(nkv + i * 512, a.k_new + row * kD, 256, bar_qfull + qs * 8);
+          bulk_load(nkv + i * 512 + 256, a.v_new + row * kD, 256, bar_qfull + qs * 8);
         }
       }
-      const int32_t* bt = a.block_tables + static_cast<int64_t>(s.b) * a.max_blocks;
+    };
+    while (has) {
+      if (!early_kv || waited) {
+        if (!waited) { griddep_wait(); waited = true; }
+        issue_q(s, k);
+      }
+      Seg nx = s;
+      const bool has_next = cur.next(nx);
       for (int cb = s.c0; cb < s.c1; cb += 32) {
+        const int32_t cur_ids = ids;
+        // prefetch the next group: the rest of this segment, or the next segment's start
+        if (cb + 32 < s.c1) ids = load_ids(s, cb + 32);
+        else if (has_next) ids = load_ids(nx, nx.c0);
         const int cc = cb + lane;
         int row = -kChunk;  // an out-of-range box: TMA fills it with zeros
         if (cc < s.c1) {
-          const int32_t phys = __ldg(bt + (cc >> a.bs_shift));
-          if (phys >= 0 && phys < a.num_blocks)
-            row = (phys * a.Hkv + s.h) * a.block_size + ((cc & chunk_mask) << 4);
+          if (cur_ids >= 0 && cur_ids < a.num_blocks)
+            row = (cur_ids * a.Hkv + s.h) * a.block_size + ((cc & chunk_mask) << 4);
           else
             atomicOr(a.err, PKV_DEVERR_BLOCK_ID);
         }
         const int n = min(32, s.c1 - cb);
         for (int l = 0; l < n; ++l, ++j) {
+          if (early_kv && !waited && j == NST) {
+            // every stage is requested; the consumers need the first queries to free one
+            griddep_wait();
+            waited = true;
+            issue_q(first_seg, 0);
+          }
           const int r = __shfl_sync(0xffffffffu, row, l);
           if (lane == 0) {
             const int st = j % NST;
@@ -482,8 +510,23 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           }
         }
       }
+      if (early_kv && !waited) {
+        // the first segment ended before the stages filled: its queries come now
+        griddep_wait();
+        waited = true;
+        issue_q(first_seg, 0);
+      }
       ++k;
-      has = cur.next(s);
+      s = nx;
+      has = has_next;
+    }
+    if (!waited) griddep_wait();
+    // sequences without any chunk get zeros (their units are in no CTA's slice)
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+      if (pre[b + 1] != pre[b]) continue;
+      const int n = a.q_len * a.Hq * kD;
+      for (int i = lane; i < n; i += 32)
+        a.out[static_cast<int64_t>(b) * n + i] = __float2half_rn(0.f);
     }
     // Before exiting, make sure no TMA write into this CTA's shared memory is still pending
     // (only matters if the consumers gave up early; otherwise these waits return at once).
@@ -531,14 +574,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       if (lane == 0) mbar_arrive(bar_sfree + sb * 8);
       if (!complete) {
         // Announce the partial. The warp barrier orders the other lanes' writes before lane
-        // 0's gpu-scope fence and arrival (release); a last arrival fences again (acquire)
-        // and leaves the merge to the end of the slice, when the whole CTA can do it.
+        // 0's arrival, a gpu-scope acquire-release atomic: the release publishes the partial,
+        // and a last arrival's acquire makes the other CTAs' partials visible. That merge waits
+        // for the end of the slice, when the whole CTA can do it.
         if (lane == 0) {
           const int ua = pre[s.b] * a.Hkv + s.h * s.nb;
           const int parts = (ua + s.nb - 1) / per - ua / per + 1;
-          __threadfence();
-          if (atomicAdd(a.counters + s.b * a.Hkv + s.h, 1) == parts - 1) {
-            __threadfence();
+          if (atomic_add_acq_rel(a.counters + s.b * a.Hkv + s.h, 1) == parts - 1) {
             npend_s[1 + 3 * npend] = s.b;
             npend_s[2 + 3 * npend] = s.h;
             npend_s[3 + 3 * npend] = s.nb;
@@ -869,9 +911,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       if (t == 0) {
         const int ua = pre[last_b] * a.Hkv + last_h * last_nb;
         const int parts = (ua + last_nb - 1) / per - ua / per + 1;
-        __threadfence();
-        if (atomicAdd(a.counters + last_b * a.Hkv + last_h, 1) == parts - 1) {
-          __threadfence();
+        if (atomic_add_acq_rel(a.counters + last_b * a.Hkv + last_h, 1) == parts - 1) {
           const int n = *npend_s;
           npend_s[1 + 3 * n] = last_b;
           npend_s[2 + 3 * n] = last_h;
@@ -1069,9 +1109,18 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   args.v_pool = static_cast<__half*>(const_cast<void*>(v_cache));
 
   void* params[4] = {&tmK, &tmV, &tmQ, &args};
-  cudaError_t e = cudaLaunchKernel(v.fn, dim3(grid), dim3((kNCW + 2) * 32), params, smem,
-                                   static_cast<cudaStream_t>(stream));
-  return cuda_status(e);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3((kNCW + 2) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  // the fused-append call may start while the preceding kernel finishes (see the kernel)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = append ? 1 : 0;
+  return cuda_status(cudaLaunchKernelExC(&cfg, v.fn, params));
 }
 
 // ---------------------------------------------------------------------------------------------
