@@ -49,6 +49,9 @@ constexpr int kStageBytes = 4 * kHalfBytes;   // K lo/hi + V lo/hi = 8 KB
 constexpr int kMaxCtasPerSm = 4;              // bounds the grid, hence the workspace
 constexpr int kMaxSeqs = 4096;
 constexpr float kNegInf = -__builtin_huge_valf();
+// How long the CTA that merges a split unit waits for the unit's other partials before it
+// falls back to announcing its own (normally they are in within microseconds).
+constexpr uint64_t kMergeWaitNs = 200000;
 
 struct DecodeArgs {
   __half* out;
@@ -91,8 +94,8 @@ struct Smem {
   static constexpr int kSrow = kFlags + 64;             // TMA row of each stage's chunk
   static constexpr int kState = kSrow + ((NST * 4 + 15) & ~15);
   // segment states handed from the consumer warps to the epilogue warp, double-buffered:
-  // o [2][NCW][R][128], m [2][NCW][R], l [2][NCW][R]; then the epilogue's weights [NCW][R]
-  __host__ __device__ static int state_floats(int R) { return 2 * NCW * R * (kD + 2) + NCW * R; }
+  // o [2][NCW][R][128], m [2][NCW][R], l [2][NCW][R]
+  __host__ __device__ static int state_floats(int R) { return 2 * NCW * R * (kD + 2); }
   __host__ __device__ static int seq_off(int R) { return kState + state_floats(R) * 4; }
   // per sequence: prefix (B+1 ints), length, high water; then (fused append) the new K/V
   // rows of the current segment, double-buffered with its queries: [2][q_len][K|V][256 B]
@@ -171,51 +174,86 @@ __device__ __forceinline__ void store_half4(__half* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
+// Weights of one row of a segment's per-warp states: w[ww] = 2^(m_ww - m) / l, with m the
+// row's max and l = sum_ww l_ww 2^(m_ww - m); returns m and l for the partial.
+template <int NCW>
+__device__ __forceinline__ void row_weights(const float* m_s, const float* l_s, int R, int r,
+                                            float (&w)[NCW], float& row_m, float& row_l) {
+  row_m = kNegInf;
+#pragma unroll
+  for (int ww = 0; ww < NCW; ++ww) {
+    w[ww] = m_s[ww * R + r];
+    row_m = fmaxf(row_m, w[ww]);
+  }
+  row_l = 0.f;
+#pragma unroll
+  for (int ww = 0; ww < NCW; ++ww) {
+    w[ww] = row_m == kNegInf ? 0.f : fast_exp2(w[ww] - row_m);
+    row_l += l_s[ww * R + r] * w[ww];
+  }
+  const float inv = row_l > 0.f ? 1.f / row_l : 0.f;
+#pragma unroll
+  for (int ww = 0; ww < NCW; ++ww) w[ww] *= inv;
+}
+
 // Merge of one segment's per-warp states (o [NCW][R][128] unnormalised, m and l [NCW][R]) into
-// the unit's output (complete segment) or its normalised partial (split unit), by NT threads
-// t = 0..NT-1. Each thread owns 4 consecutive dims of a row (float4 in, 8 bytes out).
+// the unit's output (complete segment) or its normalised partial (split unit: rows of 128
+// floats at po, rows of (m, l, 0, 0) at pml; global or shared memory), by NT threads
+// t = 0..NT-1. Each thread owns 4 consecutive dims of a row (float4 in, 8 bytes out). One warp
+// (NT == 32) forms each row's weights once, in lane r, and shares them by shuffle; a larger
+// group has each thread form its own row's weights (the same arithmetic), with no barrier.
 template <int NCW, int NT>
 __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const float* o_s,
-                                              const float* m_s, const float* l_s, float* ew,
-                                              int b, int h, bool complete, int slot, int t) {
+                                              const float* m_s, const float* l_s, int b, int h,
+                                              bool complete, float* po, float* pml, int t) {
   const int R = a.R;
-  if (t < R) {
-    float mw[NCW], row_m = kNegInf;
-#pragma unroll
-    for (int ww = 0; ww < NCW; ++ww) {
-      mw[ww] = m_s[ww * R + t];
-      row_m = fmaxf(row_m, mw[ww]);
-    }
-    float row_l = 0.f;
-#pragma unroll
-    for (int ww = 0; ww < NCW; ++ww) {
-      mw[ww] = row_m == kNegInf ? 0.f : fast_exp2(mw[ww] - row_m);
-      row_l += l_s[ww * R + t] * mw[ww];
-    }
-    const float inv = row_l > 0.f ? 1.f / row_l : 0.f;
-#pragma unroll
-    for (int ww = 0; ww < NCW; ++ww) ew[ww * R + t] = mw[ww] * inv;
-    if (!complete)
-      *reinterpret_cast<float4*>(a.part_ml + (static_cast<int64_t>(slot) * R + t) * 4) =
-          make_float4(row_m, row_l, 0.f, 0.f);
+  float w_own[NCW], m_own = 0.f, l_own = 0.f;
+  if (NT == 32 && t < R) {
+    row_weights<NCW>(m_s, l_s, R, t, w_own, m_own, l_own);
+    if (!complete) *reinterpret_cast<float4*>(pml + t * 4) = make_float4(m_own, l_own, 0.f, 0.f);
   }
-  merge_sync<NT>();
-#pragma unroll 2
+#pragma unroll 1
   for (int gi = t; gi < R * 32; gi += NT) {
     const int r = gi >> 5, c4 = gi & 31;
+    float w[NCW];
+    if (NT == 32) {
+#pragma unroll
+      for (int ww = 0; ww < NCW; ++ww) w[ww] = __shfl_sync(0xffffffffu, w_own[ww], r);
+    } else {
+      float row_m, row_l;
+      row_weights<NCW>(m_s, l_s, R, r, w, row_m, row_l);
+      if (!complete && c4 == 0)
+        *reinterpret_cast<float4*>(pml + r * 4) = make_float4(row_m, row_l, 0.f, 0.f);
+    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int ww = 0; ww < NCW; ++ww) {
       const float4 v = reinterpret_cast<const float4*>(o_s + (ww * R + r) * kD)[c4];
-      const float wt = ew[ww * R + r];
+      const float wt = w[ww];
       acc.x += wt * v.x; acc.y += wt * v.y; acc.z += wt * v.z; acc.w += wt * v.w;
     }
     if (complete)
       store_half4(out_row(a, b, h, r) + c4 * 4, acc);
     else
-      reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(slot) * R + r) * kD)[c4] = acc;
+      reinterpret_cast<float4*>(po + r * kD)[c4] = acc;
   }
 }
+
+// Where merge_unit stages partials in the (free) pipeline stage memory.
+struct MergeStage {
+  float* accv;    // [R][128] running output
+  float* rowml;   // [2][R][2] running (max, sum)
+  float* so;      // [PB][R][128] partials' o
+  float* sml;     // [PB][R][4] partials' (m, l, -, -)
+  int PB;         // partials per batch (>= 2)
+  __device__ MergeStage(uint8_t* stage_mem, int stage_bytes, int R) {
+    accv = reinterpret_cast<float*>(stage_mem);
+    rowml = accv + R * kD;
+    PB = (stage_bytes - (R * kD + 4 * R) * 4) / (R * (kD + 4) * 4);
+    so = rowml + 4 * R;
+    sml = so + PB * R * kD;
+  }
+};
 
 // Merge of a split unit's partials, run cooperatively by NT threads of the last CTA to arrive
 // on the unit's counter, after its whole slice is done (so its pipeline stages are free).
@@ -224,21 +262,22 @@ __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const float* 
 // order. The partials are copied into the stage memory with cp.async (as many per batch as fit,
 // usually all: one round trip to L2); each thread then reduces its own 4 output dims in one
 // pass, recomputing its row's weights, with no barrier inside a batch.
+// own >= 0: the unit's first partial (own == cf, the merging CTA's own) is already in the
+// staging area, at index 0 of the first batch; it is not copied from the workspace.
 template <int NT>
 __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, int nb,
                                            const int* pre, int per, uint8_t* stage_mem,
-                                           int stage_bytes, int t) {
+                                           int stage_bytes, int t, int own = -1) {
   const int R = a.R;
   const int ua = pre[b] * a.Hkv + h * nb;
   const int cf = ua / per, cl = (ua + nb - 1) / per;
   const bool first_odd = ua != cf * per;
-  float* accv = reinterpret_cast<float*>(stage_mem);       // [R][128] running output
-  float* rowml = accv + R * kD;                            // [2][R][2] running (max, sum)
-  uint8_t* rest = reinterpret_cast<uint8_t*>(rowml + 4 * R);
-  const int part_bytes = R * (kD + 4) * 4;                 // o rows and (m, l, -, -) rows
-  const int PB = (stage_bytes - (R * kD + 4 * R) * 4) / part_bytes;   // >= 2
-  float* so = reinterpret_cast<float*>(rest);              // [PB][R][128]
-  float* sml = so + PB * R * kD;                           // [PB][R][4]
+  const MergeStage ms(stage_mem, stage_bytes, R);
+  float* accv = ms.accv;
+  float* rowml = ms.rowml;
+  const int PB = ms.PB;
+  float* so = ms.so;
+  float* sml = ms.sml;
   const uint32_t so_s = smem_u32(so), sml_s = smem_u32(sml);
   const int o_vec = R * kD / 4;                            // 16-byte pieces of one partial's o
   int batch = 0;
@@ -254,6 +293,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
       const int per_part = is_o ? o_vec : R;
       const int p = j / per_part, off = j - p * per_part;
       const int cc = base + p;
+      if (cc == own) continue;
       const int64_t sl = 2 * cc + ((cc == cf && first_odd) ? 1 : 0);
       if (is_o)
         cp_async_16(so_s + (p * R * kD + off * 4) * 4, a.part_o + sl * R * kD + off * 4);
@@ -334,10 +374,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kFlags);
   int* srow_s = reinterpret_cast<int*>(smem + L::kSrow);
   int* npend_s = reinterpret_cast<int*>(smem + L::kFlags) + 1;   // then 2 x (b, h, nb)
+  volatile int* fast_s = reinterpret_cast<volatile int*>(smem + L::kFlags) + 8;
   float* stO = reinterpret_cast<float*>(smem + L::kState);     // [2][NCW][R][128]
   float* stM = stO + 2 * NCW * a.R * kD;                        // [2][NCW][R]
   float* stL = stM + 2 * NCW * a.R;                             // [2][NCW][R]
-  float* ew = stL + 2 * NCW * a.R;                              // [NCW][R] epilogue weights
   int* pre = reinterpret_cast<int*>(smem + L::seq_off(a.R));
   int* slen = pre + a.num_seqs + 1;   // ctx (paged) or L (ring), clamped
   int* shw = slen + a.num_seqs;       // ring: high water
@@ -541,7 +581,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 
   // the CTA's last segment (merged at the end by consumers and epilogue together)
   int last_k = -1, last_b = 0, last_h = 0, last_nb = 0, last_slot = 0;
-  bool last_complete = true;
+  bool last_complete = true, last_head = false;
   {
     Seg s;
     bool has = cur.first(begin, s);
@@ -550,6 +590,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       last_k = kk;
       last_b = s.b; last_h = s.h; last_nb = s.nb;
       last_complete = (s.c0 == 0 && s.c1 == s.nb);
+      last_head = s.c0 == 0;
       last_slot = 2 * blockIdx.x + (kk == 0 ? 0 : 1);
       ++kk;
       has = cur.next(s);
@@ -569,7 +610,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       const bool complete = (s.c0 == 0 && s.c1 == s.nb);
       const int slot = 2 * blockIdx.x + (k == 0 ? 0 : 1);
       merge_segment<NCW, 32>(a, stO + sb * NCW * a.R * kD, stM + sb * NCW * a.R,
-                             stL + sb * NCW * a.R, ew, s.b, s.h, complete, slot, lane);
+                             stL + sb * NCW * a.R, s.b, s.h, complete,
+                             a.part_o + static_cast<int64_t>(slot) * a.R * kD,
+                             a.part_ml + static_cast<int64_t>(slot) * a.R * 4, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_sfree + sb * 8);
       if (!complete) {
@@ -902,22 +945,60 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   // whose last partial arrived from this CTA (the producer has left)
   if (warp != NCW && last_k >= 0) {
     const int t = warp < NCW ? tid : tid - 32;   // dense index over consumers + epilogue
+    const int ua = pre[last_b] * a.Hkv + last_h * last_nb;
+    const int parts = (ua + last_nb - 1) / per - ua / per + 1;
+    const MergeStage ms(smem, NST * kStageBytes, a.R);
     named_barrier_sync(2, kNE);                  // last states written, earlier segments merged
     const int sb = last_k & 1;
-    merge_segment<NCW, kNE>(a, stO + sb * NCW * a.R * kD, stM + sb * NCW * a.R,
-                            stL + sb * NCW * a.R, ew, last_b, last_h, last_complete, last_slot, t);
-    if (!last_complete) {
-      named_barrier_sync(2, kNE);                // partial written by every thread
+    const float* so_w = stO + sb * NCW * a.R * kD;
+    const float* sm_w = stM + sb * NCW * a.R;
+    const float* sl_w = stL + sb * NCW * a.R;
+    int* counter = a.counters + last_b * a.Hkv + last_h;
+    // A split unit is merged by the CTA that holds its first chunk, the one whose last segment
+    // is the unit's head. That CTA keeps its own partial in the staging area (it never goes out
+    // to the workspace and back) and waits until the other CTAs have announced theirs; most of
+    // them finished that work long before (a unit's other parts are the first segments of
+    // later CTAs, or whole slices). The wait is bounded in time: if the other parts are not in
+    // (their CTAs may not be resident yet, e.g. when other work holds the GPU), the CTA
+    // announces its partial like the others and the last to arrive merges. Either way the
+    // partials and their order are the same, so the result does not depend on the path.
+    bool merged = false;
+    if (!last_complete && last_head) {
+      merge_segment<NCW, kNE>(a, so_w, sm_w, sl_w, last_b, last_h, false, ms.so, ms.sml, t);
       if (t == 0) {
-        const int ua = pre[last_b] * a.Hkv + last_h * last_nb;
-        const int parts = (ua + last_nb - 1) / per - ua / per + 1;
-        if (atomic_add_acq_rel(a.counters + last_b * a.Hkv + last_h, 1) == parts - 1) {
-          const int n = *npend_s;
-          npend_s[1 + 3 * n] = last_b;
-          npend_s[2 + 3 * n] = last_h;
-          npend_s[3 + 3 * n] = last_nb;
-          *npend_s = n + 1;
-        }
+        const uint64_t t_end = global_time_ns() + kMergeWaitNs;
+        int ok = 0;
+        do {
+          if (ld_acquire_gpu(counter) == parts - 1) { ok = 1; break; }
+        } while (global_time_ns() < t_end);
+        *fast_s = ok;
+      }
+      named_barrier_sync(2, kNE);
+      merged = *fast_s;
+      if (merged) {
+        merge_unit<kNE>(a, last_b, last_h, last_nb, pre, per, smem, NST * kStageBytes, t,
+                        blockIdx.x);
+      } else {
+        // give up waiting: the staged partial goes to the workspace like the others'
+        float* po = a.part_o + static_cast<int64_t>(last_slot) * a.R * kD;
+        float* pml = a.part_ml + static_cast<int64_t>(last_slot) * a.R * 4;
+        for (int i = t; i < a.R * 32; i += kNE)
+          reinterpret_cast<float4*>(po)[i] = reinterpret_cast<const float4*>(ms.so)[i];
+        if (t < a.R) reinterpret_cast<float4*>(pml)[t] = reinterpret_cast<const float4*>(ms.sml)[t];
+      }
+    } else {
+      merge_segment<NCW, kNE>(a, so_w, sm_w, sl_w, last_b, last_h, last_complete,
+                              a.part_o + static_cast<int64_t>(last_slot) * a.R * kD,
+                              a.part_ml + static_cast<int64_t>(last_slot) * a.R * 4, t);
+    }
+    if (!last_complete && !merged) {
+      named_barrier_sync(2, kNE);                // partial written by every thread
+      if (t == 0 && atomic_add_acq_rel(counter, 1) == parts - 1) {
+        const int n = *npend_s;
+        npend_s[1 + 3 * n] = last_b;
+        npend_s[2 + 3 * n] = last_h;
+        npend_s[3 + 3 * n] = last_nb;
+        *npend_s = n + 1;
       }
     }
     named_barrier_sync(2, kNE);
@@ -984,7 +1065,11 @@ int grid_size(const Variant& v, size_t smem, int* status) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, (kNCW + 2) * 32, smem);
   if (e != cudaSuccess) { *status = cuda_status(e); return 0; }
   if (occ < 1) { *status = PKV_EINVAL; return 0; }
+#ifdef PKV_CTAS_PER_SM
+  const int grid = sm_count() * std::min(std::min(occ, kMaxCtasPerSm), PKV_CTAS_PER_SM);
+#else
   const int grid = sm_count() * std::min(occ, kMaxCtasPerSm);
+#endif
   cache[key] = grid;
   return grid;
 }

@@ -174,6 +174,19 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
   return old;
 }
 
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_time_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
 
 // 16-byte global -> shared copy that bypasses L1 (Ampere-style cp.async), and its wait.
