@@ -1,9 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of paged decode attention on one GPU (or N data-parallel replicas).
 
-One step is one decode step of the whole attention stack of the workload: slot mapping of
-the step's new tokens, then for every layer the KV append and the paged decode attention,
-all through the C ABI of libpkv.so, captured once in a CUDA graph and replayed.
+One step is one decode step of the whole attention stack of the workload: for every layer
+one fused launch that writes the step's new K/V rows to the slots the block table maps their
+positions to (slot mapping + KV append) and runs the paged decode attention, all through the
+C ABI of libpkv.so, captured once in a CUDA graph and replayed.
 
 Printed (rank 0, one JSON line): the KV-read bandwidth (algorithmic fp16 K+V bytes the step
 reads over the step time), decode tokens/s, the decode kernel's roofline against the
@@ -350,14 +351,15 @@ def cpu_baseline(w, budget_s):
     import oracle
     oracle.build()
     secs, nbytes, threads = oracle_sample(w, range(w.num_seqs), [0])
-    layers = 1
-    while layers < w.num_layers and secs * (layers + 1) / layers < budget_s:
-        s, b, threads = oracle_sample(w, range(w.num_seqs), [layers])
+    layers = 1   # layer evaluations, cycling over the workload's layers
+    while secs * (layers + 1) / layers < budget_s:
+        s, b, threads = oracle_sample(w, range(w.num_seqs), [layers % w.num_layers])
         secs, nbytes, layers = secs + s, nbytes + b, layers + 1
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"{layers} of {w.num_layers} layers, all {w.num_seqs} sequences "
-                      f"(append + fp64 attention), {secs:.1f} s"}
+            "sample": f"{layers} layer evaluations ({layers / w.num_layers:.1f} passes over the "
+                      f"{w.num_layers} layers), all {w.num_seqs} sequences (append + fp64 "
+                      f"attention), {secs:.1f} s"}
 
 
 def run_reference(args, w, world_size):
