@@ -48,6 +48,9 @@ constexpr int kHalfBytes = kChunk * 128;      // 16 rows x 64 dims x 2 B (one sw
 constexpr int kStageBytes = 4 * kHalfBytes;   // K lo/hi + V lo/hi = 8 KB
 constexpr int kMaxCtasPerSm = 4;              // bounds the grid, hence the workspace
 constexpr int kMaxSeqs = 4096;
+// Row stride (floats) of the per-warp output states in shared memory: 8 floats of padding put
+// the 8 rows a warp's float2 stores touch at once in different banks.
+constexpr int kSt = kD + 8;
 constexpr float kNegInf = -__builtin_huge_valf();
 // How long the CTA that merges a split unit waits for the unit's other partials before it
 // falls back to announcing its own (normally they are in within microseconds).
@@ -94,8 +97,8 @@ struct Smem {
   static constexpr int kSrow = kFlags + 64;             // TMA row of each stage's chunk
   static constexpr int kState = kSrow + ((NST * 4 + 15) & ~15);
   // segment states handed from the consumer warps to the epilogue warp, double-buffered:
-  // o [2][NCW][R][128], m [2][NCW][R], l [2][NCW][R]
-  __host__ __device__ static int state_floats(int R) { return 2 * NCW * R * (kD + 2); }
+  // o [2][NCW][R][kSt] (128 used), m [2][NCW][R], l [2][NCW][R]
+  __host__ __device__ static int state_floats(int R) { return 2 * NCW * R * (kSt + 2); }
   __host__ __device__ static int seq_off(int R) { return kState + state_floats(R) * 4; }
   // per sequence: prefix (B+1 ints), length, high water; then (fused append) the new K/V
   // rows of the current segment, double-buffered with its queries: [2][q_len][K|V][256 B]
@@ -196,8 +199,9 @@ __device__ __forceinline__ void row_weights(const float* m_s, const float* l_s, 
   for (int ww = 0; ww < NCW; ++ww) w[ww] *= inv;
 }
 
-// Merge of one segment's per-warp states (o [NCW][R][128] unnormalised, m and l [NCW][R]) into
-// the unit's output (complete segment) or its normalised partial (split unit: rows of 128
+// Merge of one segment's per-warp states (o: [NCW][R] rows of kSt floats, unnormalised; m and
+// l: [NCW][R]) into the unit's output (complete segment) or its normalised partial (split
+// unit: rows of 128
 // floats at po, rows of (m, l, 0, 0) at pml; global or shared memory), by NT threads
 // t = 0..NT-1. Each thread owns 4 consecutive dims of a row (float4 in, 8 bytes out). One warp
 // (NT == 32) forms each row's weights once, in lane r, and shares them by shuffle; a larger
@@ -228,7 +232,7 @@ __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const float* 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int ww = 0; ww < NCW; ++ww) {
-      const float4 v = reinterpret_cast<const float4*>(o_s + (ww * R + r) * kD)[c4];
+      const float4 v = reinterpret_cast<const float4*>(o_s + (ww * R + r) * kSt)[c4];
       const float wt = w[ww];
       acc.x += wt * v.x; acc.y += wt * v.y; acc.z += wt * v.z; acc.w += wt * v.w;
     }
@@ -375,8 +379,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   int* srow_s = reinterpret_cast<int*>(smem + L::kSrow);
   int* npend_s = reinterpret_cast<int*>(smem + L::kFlags) + 1;   // then 2 x (b, h, nb)
   volatile int* fast_s = reinterpret_cast<volatile int*>(smem + L::kFlags) + 8;
-  float* stO = reinterpret_cast<float*>(smem + L::kState);     // [2][NCW][R][128]
-  float* stM = stO + 2 * NCW * a.R * kD;                        // [2][NCW][R]
+  float* stO = reinterpret_cast<float*>(smem + L::kState);     // [2][NCW][R][kSt]
+  float* stM = stO + 2 * NCW * a.R * kSt;                       // [2][NCW][R]
   float* stL = stM + 2 * NCW * a.R;                             // [2][NCW][R]
   int* pre = reinterpret_cast<int*>(smem + L::seq_off(a.R));
   int* slen = pre + a.num_seqs + 1;   // ctx (paged) or L (ring), clamped
@@ -609,7 +613,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       if (!mbar_wait(bar_sdone + sb * 8, (k >> 1) & 1, abort)) flag_timeout(a, abort);
       const bool complete = (s.c0 == 0 && s.c1 == s.nb);
       const int slot = 2 * blockIdx.x + (k == 0 ? 0 : 1);
-      merge_segment<NCW, 32>(a, stO + sb * NCW * a.R * kD, stM + sb * NCW * a.R,
+      merge_segment<NCW, 32>(a, stO + sb * NCW * a.R * kSt, stM + sb * NCW * a.R,
                              stL + sb * NCW * a.R, s.b, s.h, complete,
                              a.part_o + static_cast<int64_t>(slot) * a.R * kD,
                              a.part_ml + static_cast<int64_t>(slot) * a.R * 4, lane);
@@ -914,7 +918,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       // ---- hand this warp's state for the segment to the epilogue warp ----
       const int sb = k & 1;
       if (k >= 2 && !mbar_wait(bar_sfree + sb * 8, ((k >> 1) - 1) & 1, abort)) flag_timeout(a, abort);
-      float* o_d = stO + sb * NCW * a.R * kD;
+      float* o_d = stO + sb * NCW * a.R * kSt;
   #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
@@ -924,7 +928,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           lv += __shfl_xor_sync(0xffffffffu, lv, 2);
           const int r = mt * 16 + rh * 8 + g;
           if (r < a.R) {
-            float* dst = o_d + (w * a.R + r) * kD + 2 * t4;
+            float* dst = o_d + (w * a.R + r) * kSt + 2 * t4;
   #pragma unroll
             for (int nd = 0; nd < 16; ++nd)
               *reinterpret_cast<float2*>(dst + nd * 8) = make_float2(o[mt][nd][rh * 2], o[mt][nd][rh * 2 + 1]);
@@ -950,7 +954,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const MergeStage ms(smem, NST * kStageBytes, a.R);
     named_barrier_sync(2, kNE);                  // last states written, earlier segments merged
     const int sb = last_k & 1;
-    const float* so_w = stO + sb * NCW * a.R * kD;
+    const float* so_w = stO + sb * NCW * a.R * kSt;
     const float* sm_w = stM + sb * NCW * a.R;
     const float* sl_w = stL + sb * NCW * a.R;
     int* counter = a.counters + last_b * a.Hkv + last_h;
