@@ -48,6 +48,13 @@ constexpr int kHalfBytes = kChunk * 128;      // 16 rows x 64 dims x 2 B (one sw
 constexpr int kStageBytes = 4 * kHalfBytes;   // K lo/hi + V lo/hi = 8 KB
 constexpr int kMaxCtasPerSm = 4;              // bounds the grid, hence the workspace
 constexpr int kMaxSeqs = 4096;
+// Per-segment cost in chunk equivalents: in the stream that is cut into equal slices, every
+// non-empty unit is preceded by this many empty positions, so a CTA whose slice holds many
+// short units (each one a segment: queries, hand-off, merge) gets fewer chunks.
+#ifndef PKV_SEGMENT_COST
+#define PKV_SEGMENT_COST 2
+#endif
+constexpr int kSegCost = PKV_SEGMENT_COST;
 // Row stride (floats) of the per-warp output states in shared memory: 8 floats of padding put
 // the 8 rows a warp's float2 stores touch at once in different banks.
 constexpr int kSt = kD + 8;
@@ -115,38 +122,51 @@ struct Seg {
   int x;                 // global stream index of chunk c0
 };
 
+// The stream: unit (b, h) of a sequence with nb > 0 chunks per kv head occupies nb + kSegCost
+// positions, kSegCost empty ones and then its chunks; pre[b] is the length (per kv head) of the
+// sequences before b, so the unit starts at pre[b] * Hkv + h * (nb + kSegCost). A CTA's slice
+// [a, end) of the stream gives it segments: the runs of chunks of one unit inside the slice.
+__device__ __forceinline__ int unit_first(const int* pre, int Hkv, int b, int h, int nb) {
+  return pre[b] * Hkv + h * (nb + kSegCost) + kSegCost;   // position of the unit's chunk 0
+}
+
 struct Cursor {
-  const int* pre;  // pre[b] = chunks (per kv head) of sequences < b
+  const int* pre;
   int B, Hkv, end;
 
   __device__ __forceinline__ bool first(int a, Seg& s) const {
     if (a >= end) return false;
-    int lo = 0, hi = B - 1;  // largest b with pre[b] * Hkv <= a
+    int lo = 0, hi = B - 1;  // largest b with pre[b] * Hkv <= a (a sequence with chunks)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (pre[mid] * Hkv <= a) lo = mid; else hi = mid - 1;
     }
-    s.b = lo;
-    s.nb = pre[lo + 1] - pre[lo];
+    const int vl = pre[lo + 1] - pre[lo];
     const int off = a - pre[lo] * Hkv;
-    s.h = off / s.nb;
-    s.c0 = off - s.h * s.nb;
-    s.c1 = min(s.nb, s.c0 + (end - a));
-    s.x = a;
+    const int h = off / vl, o = off - h * vl;
+    const int ustart = a - o;
+    const int x0 = ustart + kSegCost + max(o - kSegCost, 0);   // first chunk in the slice
+    if (x0 >= end) return false;   // the slice ends before the unit's first chunk
+    s.b = lo;
+    s.h = h;
+    s.nb = vl - kSegCost;
+    s.c0 = x0 - ustart - kSegCost;
+    s.c1 = min(s.nb, end - ustart - kSegCost);
+    s.x = x0;
     return true;
   }
   __device__ __forceinline__ bool next(Seg& s) const {
-    const int x = s.x + (s.c1 - s.c0);
-    if (x >= end) return false;
-    // the previous segment ended its unit (it stopped short of `end`)
+    // the next unit's first chunk, if the slice reaches it (then this segment ended its unit)
+    const int u2 = s.x - s.c0 + s.nb;
+    if (u2 + kSegCost >= end) return false;
     if (++s.h == Hkv) {
       s.h = 0;
       do { ++s.b; } while (pre[s.b + 1] == pre[s.b]);
     }
-    s.nb = pre[s.b + 1] - pre[s.b];
+    s.nb = pre[s.b + 1] - pre[s.b] - kSegCost;
     s.c0 = 0;
-    s.c1 = min(s.nb, end - x);
-    s.x = x;
+    s.c1 = min(s.nb, end - (u2 + kSegCost));
+    s.x = u2 + kSegCost;
     return true;
   }
 };
@@ -273,9 +293,11 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
                                            const int* pre, int per, uint8_t* stage_mem,
                                            int stage_bytes, int t, int own = -1) {
   const int R = a.R;
-  const int ua = pre[b] * a.Hkv + h * nb;
+  const int ua = unit_first(pre, a.Hkv, b, h, nb);
   const int cf = ua / per, cl = (ua + nb - 1) / per;
-  const bool first_odd = ua != cf * per;
+  // the unit is not the first segment of slice cf if that slice reaches back into the unit
+  // before it (whose last chunk is the position just before this unit's empty ones)
+  const bool first_odd = cf * per < ua - kSegCost;
   const MergeStage ms(stage_mem, stage_bytes, R);
   float* accv = ms.accv;
   float* rowml = ms.rowml;
@@ -414,7 +436,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     }
     slen[b] = len;
     shw[b] = hw;
-    pre[b + 1] = nchunks;  // scanned below
+    pre[b + 1] = nchunks > 0 ? nchunks + kSegCost : 0;  // scanned below
   }
   // zero both Q buffers so rows past R are finite; TMA overwrites rows < R
   for (int i = tid; i < L::kQBuf * 2 / 16; i += blockDim.x)
@@ -625,7 +647,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         // and a last arrival's acquire makes the other CTAs' partials visible. That merge waits
         // for the end of the slice, when the whole CTA can do it.
         if (lane == 0) {
-          const int ua = pre[s.b] * a.Hkv + s.h * s.nb;
+          const int ua = unit_first(pre, a.Hkv, s.b, s.h, s.nb);
           const int parts = (ua + s.nb - 1) / per - ua / per + 1;
           if (atomic_add_acq_rel(a.counters + s.b * a.Hkv + s.h, 1) == parts - 1) {
             npend_s[1 + 3 * npend] = s.b;
@@ -949,7 +971,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   // whose last partial arrived from this CTA (the producer has left)
   if (warp != NCW && last_k >= 0) {
     const int t = warp < NCW ? tid : tid - 32;   // dense index over consumers + epilogue
-    const int ua = pre[last_b] * a.Hkv + last_h * last_nb;
+    const int ua = unit_first(pre, a.Hkv, last_b, last_h, last_nb);
     const int parts = (ua + last_nb - 1) / per - ua / per + 1;
     const MergeStage ms(smem, NST * kStageBytes, a.R);
     named_barrier_sync(2, kNE);                  // last states written, earlier segments merged
@@ -1134,7 +1156,7 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   // all chunk indices and TMA rows fit in int32
   const int64_t rows = static_cast<int64_t>(num_blocks) * Hkv * block_size;
   const int64_t max_ctx = ring ? (sink + window) : static_cast<int64_t>(max_blocks) * block_size;
-  if (rows >= (1ll << 31) || static_cast<int64_t>(num_seqs) * Hkv * ((max_ctx + kChunk - 1) / kChunk) >= (1ll << 30))
+  if (rows >= (1ll << 31) || static_cast<int64_t>(num_seqs) * Hkv * ((max_ctx + kChunk - 1) / kChunk + kSegCost) >= (1ll << 30))
     return PKV_EINVAL;
   if (num_blocks == 0) return PKV_EINVAL;
   const WsLayout ws = ws_layout(num_seqs, Hkv, R);
