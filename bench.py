@@ -48,7 +48,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=30)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="edge_1p1b",
-                    choices=["edge_1p1b", "llama70b_b16", "llama70b_mixed"])
+                    choices=["edge_1p1b", "llama70b_b16", "llama70b_mixed", "prefix", "ring"],
+                    help="prefix: the shared-prefix MHA batch, decode only (its forked children "
+                         "share their last block, so there is no append); ring: the sink + "
+                         "ring cache over 24 layers, 4 draft queries per sequence")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -66,17 +69,39 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def step_bytes(w) -> int:
+    """Algorithmic fp16 K+V bytes one step reads over all layers: every visible token of every
+    (sequence, kv head) once (for the ring, the min(hw, sink + window) slots it holds)."""
+    if w.name == "ring":
+        hw = w.context_lens.astype(np.int64)          # L = hw: no rollback in this step
+        toks = int(np.minimum(hw, w.sink + w.window).sum())
+        return toks * w.num_kv_heads * w.head_dim * 2 * 2 * w.num_layers
+    return w.kv_read_bytes()
+
+
+def unique_bytes(w) -> int:
+    """K+V bytes of the distinct physical block rows a step reads (shared blocks once)."""
+    used = {}
+    for b in range(w.num_seqs):
+        n = int(w.context_lens[b])
+        for j in range((n + w.block_size - 1) // w.block_size):
+            blk = int(w.block_tables[b, j])
+            used[blk] = max(used.get(blk, 0), min(w.block_size, n - j * w.block_size))
+    return sum(used.values()) * w.num_kv_heads * w.head_dim * 2 * 2 * w.num_layers
+
+
 def describe(w) -> dict:
     cl = w.context_lens.astype(np.int64)
+    nbytes = step_bytes(w)
     return {
         "workload": w.name,
         "layers": w.num_layers, "num_seqs": w.num_seqs, "q_len": w.q_len,
         "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
         "block_size": w.block_size, "pool_blocks_per_layer": w.num_blocks,
         "context_min_mean_max": [int(cl.min()), round(float(cl.mean()), 1), int(cl.max())],
-        "kv_bytes_per_step": w.kv_read_bytes(),
+        "kv_bytes_per_step": nbytes,
         "accumulate": "f32",
-        "l2": f"no flush: one step reads {w.kv_read_bytes() / 1e9:.2f} GB of K/V, "
+        "l2": f"no flush: one step reads {nbytes / 1e9:.2f} GB of K/V, "
               f"more than the {L2_BYTES / 2**20:.0f} MiB L2",
     }
 
@@ -140,6 +165,9 @@ class Step:
         self.pkv = pkv
         self.w = w
         self.dev = dev
+        # fused append + decode per layer (paged workloads), decode only (prefix), or the
+        # sink + ring decode (ring)
+        self.kind = {"prefix": "decode", "ring": "ring"}.get(w.name, "fused")
         Lr = w.num_layers
         self.k, self.v = w.pools(dev)
         self.bt = torch.as_tensor(w.block_tables, device=dev)
@@ -155,23 +183,54 @@ class Step:
         self.slots = torch.empty(seq.shape[0], dtype=torch.int64, device=dev)
         self.ws = pkv.make_workspace(w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, dev)
         self.launches_per_step = Lr
+        if self.kind == "ring":
+            self.L = torch.as_tensor(w.context_lens.astype(np.int64), device=dev)
+            self.hw = self.L.clone()
+            self.rope = pkv.rope_table(w.sink + w.window).to(dev)
 
     def run(self):
         """One decode step: per layer, the fused call appends the new K/V rows at the slots the
         block table gives (slot mapping + append) and runs paged decode attention."""
         p, w = self.pkv, self.w
+        if self.kind == "decode":
+            return self.run_decode_only()
         for l in range(w.num_layers):
-            p.paged_attn_decode_append(self.out[l], self.q[l], self.kn[l], self.vn[l], self.k[l],
-                                       self.v[l], self.bt, self.cl, w.scale, self.ws)
+            if self.kind == "ring":
+                p.ring_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.L,
+                                   self.hw, w.sink, w.window, self.rope, w.scale, self.ws)
+            else:
+                p.paged_attn_decode_append(self.out[l], self.q[l], self.kn[l], self.vn[l],
+                                           self.k[l], self.v[l], self.bt, self.cl, w.scale,
+                                           self.ws)
 
     def run_decode_only(self):
         p, w = self.pkv, self.w
+        if self.kind == "ring":
+            return self.run()
         for l in range(w.num_layers):
             p.paged_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.cl,
                                 w.scale, self.ws)
 
     def h2d_sources(self):
+        if self.kind == "decode":
+            return [self.q, self.bt, self.cl]
+        if self.kind == "ring":
+            return [self.q, self.bt, self.L, self.hw]
         return [self.q, self.kn, self.vn, self.bt, self.cl, self.seq, self.pos]
+
+    def graph_note(self) -> str:
+        n = self.w.num_layers
+        if self.kind == "decode":
+            return f"CUDA graph: {n} x paged_attn_decode (decode only)"
+        if self.kind == "ring":
+            return f"CUDA graph: {n} x ring_attn_decode ({self.w.q_len} causal draft queries)"
+        return (f"CUDA graph: {n} x paged_attn_decode_append "
+                "(slot mapping + KV append + decode, one launch)")
+
+    def kernel_note(self) -> str:
+        return {"decode": "decode_kernel (paged_attn_decode)",
+                "ring": "decode_kernel, sink + ring with RoPE on read (ring_attn_decode)"}.get(
+            self.kind, "decode_kernel, fused append (paged_attn_decode_append)")
 
 
 def capture(fn):
@@ -232,16 +291,17 @@ def run_ours(args, w, rank, local_rank, world_size):
     clocks.start()
     elapsed = time_replays(step_graph, args.steps, args.warmup)
     clk = clocks.stop()
-    bytes_step = w.kv_read_bytes()
+    bytes_step = step_bytes(w)
     t_max, total_bytes = replicas.aggregate(elapsed, float(bytes_step) * args.steps,
                                             device=dev)
     value = total_bytes / t_max / 1e9
 
-    # dominant kernel: the fused decode (slot mapping + append + attention) is the whole step;
-    # its average launch duration is the step time over its launches (they run back to back,
-    # each overlapping the previous one's tail). The unfused decode is timed alone as well.
+    # dominant kernel: the decode launch is the whole step; its average launch duration is
+    # the step time over its launches (they run back to back, the fused ones each overlapping
+    # the previous one's tail). The unfused decode is timed alone as well. For the prefix batch
+    # the roofline counts the distinct block rows (the shared prefix once).
     per_launch = (t_max / args.steps) / w.num_layers
-    bytes_launch = bytes_step / w.num_layers
+    bytes_launch = (unique_bytes(w) if w.name == "prefix" else bytes_step) / w.num_layers
     peak, peak_kind = load_peaks()
     achieved = bytes_launch / per_launch / 1e9
     traffic = traffic_record(w)
@@ -290,21 +350,23 @@ def run_ours(args, w, rank, local_rank, world_size):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t_max / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": describe(w) | {"graph": f"CUDA graph: {w.num_layers} x paged_attn_decode_append "
-                                          "(slot mapping + KV append + decode, one launch)",
+        "config": describe(w) | {"graph": st.graph_note(),
                                  "parallelism": f"replicas x{world_size}"},
         "decode_tokens_per_s": round(w.num_seqs * w.q_len * args.steps * world_size / t_max, 1),
         "pct_of_nominal_8tbs": round(100 * value / world_size / NOMINAL_HBM_GBS, 2),
         f"pct_of_{peak_kind}_hbm": round(100 * value / world_size / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_kernel, fused append (paged_attn_decode_append)",
+                     "kernel": st.kernel_note(),
                      "launch_us": round(per_launch * 1e6, 3),
                      "unfused_decode_launch_us": round(plain_per_launch * 1e6, 3),
                      "algorithmic_bytes_per_launch": int(bytes_launch),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": e2e,
         "gpu_launches": st.launches_per_step * args.steps,
+        **({"unique_kv_bytes_per_step": unique_bytes(w),
+            "unique_gbs": round(unique_bytes(w) * args.steps * world_size / t_max / 1e9, 2)}
+           if w.name == "prefix" else {}),
         "clocks": clk,
     }
     return line
@@ -396,7 +458,9 @@ def run_reference(args, w, world_size):
 def main():
     args = parse_args()
     rank, local_rank, world_size = replicas.world()
-    w = workloads.WORKLOADS[args.workload]()
+    # the ring cache spans 24 layers of the 1.1B shape, so that a step exceeds L2
+    w = workloads.ring(num_layers=24) if args.workload == "ring" else \
+        workloads.WORKLOADS[args.workload]()
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w, world_size)), flush=True)
@@ -404,7 +468,7 @@ def main():
     replicas.init()
     line = run_ours(args, w, rank, local_rank, world_size)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and w.name != "ring":
             line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     replicas.shutdown()
