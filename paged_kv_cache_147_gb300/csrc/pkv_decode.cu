@@ -738,6 +738,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       for (int jj = ((w - j) % NCW + NCW) % NCW; jj < nchunk; jj += NCW) {
         const int gj = j + jj;
         const int st = gj % NST;
+        if (RING) {
+          // the RoPE rows of this chunk's 16 keys (512 B each) start towards L1 while the
+          // chunk's tiles land: two lines per lane
+          const int t = (s.c0 + jj) * kChunk + (lane >> 1);
+          int jr = -1;
+          if (t < a.sink) jr = t;
+          else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; jr = a.sink + d; }
+          if (jr >= 0) {
+            const float* row = a.rope + jr * 128 + (lane & 1) * 64;
+            prefetch_l1(row);
+            prefetch_l1(row + 32);
+          }
+        }
         if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
         const uint32_t stK = sbase + st * kStageBytes;
         const uint32_t stV = stK + 2 * kHalfBytes;

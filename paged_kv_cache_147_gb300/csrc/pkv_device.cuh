@@ -174,6 +174,11 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
   return old;
 }
 
+// Prefetch of the 128-byte line holding p into L1.
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // Nanoseconds of the GPU's global timer.
 __device__ __forceinline__ uint64_t global_time_ns() {
   uint64_t t;
