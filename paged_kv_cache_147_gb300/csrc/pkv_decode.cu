@@ -61,7 +61,10 @@ constexpr int kSt = kD + 8;
 constexpr float kNegInf = -__builtin_huge_valf();
 // How long the CTA that merges a split unit waits for the unit's other partials before it
 // falls back to announcing its own (normally they are in within microseconds).
-constexpr uint64_t kMergeWaitNs = 200000;
+#ifndef PKV_MERGE_WAIT_NS
+#define PKV_MERGE_WAIT_NS 200000
+#endif
+constexpr uint64_t kMergeWaitNs = PKV_MERGE_WAIT_NS;
 
 struct DecodeArgs {
   __half* out;

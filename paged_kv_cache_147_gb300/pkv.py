@@ -55,35 +55,45 @@ def load() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                                "`python -m paged_kv_cache_147_gb300.build` (no CPU fallback)")
-        lib = ctypes.CDLL(LIB_PATH)
-        P, i32, i64, sz, f32, f64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
-                                     ctypes.c_size_t, ctypes.c_float, ctypes.c_double)
-        sig = {
-            "pkv_version": (i32, []),
-            "pkv_device_error": (i32, [P, i32, P]),
-            "pkv_slot_mapping": (i32, [P, P, i32, P, i32, i32, i32, P, P]),
-            "pkv_ring_slot_mapping": (i32, [P, P, i32, P, i32, i32, i32, i32, i32, P, P]),
-            "pkv_kv_append": (i32, [P, P, P, i32, P, P, i32, i32, i32, i32, P]),
-            "pkv_copy_blocks": (i32, [P, P, P, P, i32, i64, i32, i32, i32, i32, i32, P]),
-            "pkv_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
-            "pkv_workspace_init": (i32, [P, sz, P]),
-            "pkv_paged_attn_decode": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32,
-                                            i32, f32, P, sz, P]),
-            "pkv_rope_table": (i32, [P, i32, i32, f64]),
-            "pkv_ring_attn_decode": (i32, [P, P, P, P, i32, P, i32, P, P, i32, i32, i32, i32,
-                                           i32, i32, i32, i32, P, f32, P, sz, P]),
-            "pkv_check_tables": (i32, [P, P, i32, i32, i32, i32, P]),
-            "pkv_check_slots": (i32, [P, i32, i32, i32, P]),
-            "pkv_paged_attn_decode_noalloc": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32,
-                                                    i32, i32, i32, f32, P]),
-            "pkv_paged_attn_decode_append": (i32, [P, P, P, P, P, P, i32, P, i32, P, i32, i32,
-                                                   i32, i32, i32, i32, f32, P, sz, P]),
-        }
-        for name, (res, args) in sig.items():
-            f = getattr(lib, name)
-            f.restype, f.argtypes = res, args
-        _lib = lib
-        return lib
+        _lib = _configure(ctypes.CDLL(LIB_PATH))
+        return _lib
+
+
+def load_variant(path: str) -> ctypes.CDLL:
+    """Loads another build of the library (e.g. one compiled with different tuning macros)
+    next to the default one, with the same signatures; the tests compare the two."""
+    return _configure(ctypes.CDLL(path))
+
+
+def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Sets the argument and result types of every entry point on a loaded library."""
+    P, i32, i64, sz, f32, f64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                 ctypes.c_size_t, ctypes.c_float, ctypes.c_double)
+    sig = {
+        "pkv_version": (i32, []),
+        "pkv_device_error": (i32, [P, i32, P]),
+        "pkv_slot_mapping": (i32, [P, P, i32, P, i32, i32, i32, P, P]),
+        "pkv_ring_slot_mapping": (i32, [P, P, i32, P, i32, i32, i32, i32, i32, P, P]),
+        "pkv_kv_append": (i32, [P, P, P, i32, P, P, i32, i32, i32, i32, P]),
+        "pkv_copy_blocks": (i32, [P, P, P, P, i32, i64, i32, i32, i32, i32, i32, P]),
+        "pkv_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
+        "pkv_workspace_init": (i32, [P, sz, P]),
+        "pkv_paged_attn_decode": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32,
+                                        i32, f32, P, sz, P]),
+        "pkv_rope_table": (i32, [P, i32, i32, f64]),
+        "pkv_ring_attn_decode": (i32, [P, P, P, P, i32, P, i32, P, P, i32, i32, i32, i32,
+                                       i32, i32, i32, i32, P, f32, P, sz, P]),
+        "pkv_check_tables": (i32, [P, P, i32, i32, i32, i32, P]),
+        "pkv_check_slots": (i32, [P, i32, i32, i32, P]),
+        "pkv_paged_attn_decode_noalloc": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32,
+                                                i32, i32, i32, f32, P]),
+        "pkv_paged_attn_decode_append": (i32, [P, P, P, P, P, P, i32, P, i32, P, i32, i32,
+                                               i32, i32, i32, i32, f32, P, sz, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    return lib
 
 
 def _check(fn: str, status: int) -> None:
