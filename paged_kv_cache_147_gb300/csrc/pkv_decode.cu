@@ -59,6 +59,20 @@ constexpr int kSegCost = PKV_SEGMENT_COST;
 // the 8 rows a warp's float2 stores touch at once in different banks.
 constexpr int kSt = kD + 8;
 constexpr float kNegInf = -__builtin_huge_valf();
+// Consumer warps and pipeline stages per CTA, and the CTAs per SM the register budget of the
+// one-m-tile kernels is sized for. Two consumer warps keep up with HBM (each takes a 16-token
+// chunk in well under a microsecond) and leave the shared memory for ten 8 KB stages per CTA,
+// two CTAs per SM: 160 KB of K/V in flight per SM.
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 2
+#endif
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 10
+#endif
+#ifndef PKV_DECODE_MIN_CTAS
+#define PKV_DECODE_MIN_CTAS 2
+#endif
+constexpr int kMinCtasMt1 = PKV_DECODE_MIN_CTAS;
 // How long the CTA that merges a split unit waits for the unit's other partials before it
 // falls back to announcing its own (normally they are in within microseconds).
 #ifndef PKV_MERGE_WAIT_NS
@@ -375,7 +389,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
 // epilogue (merges each segment's per-warp states, writes outputs and split-unit partials,
 // announces arrivals), so the consumers never stop at a unit boundary.
 template <int NCW, int NST, int MT, bool RING, bool APPEND>
-__global__ void __launch_bounds__((NCW + 2) * 32, (MT == 1 && NCW <= 4) ? 2 : 1)
+__global__ void __launch_bounds__((NCW + 2) * 32, MT == 1 ? kMinCtasMt1 : 1)
 decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
   using L = Smem<NCW, NST, MT>;
@@ -1055,14 +1069,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 
 // ---------------------------------------------------------------------------------------------
 // Host side.
-#ifndef PKV_DECODE_WARPS
-#define PKV_DECODE_WARPS 4
-#endif
-#ifndef PKV_DECODE_STAGES
-#define PKV_DECODE_STAGES 8
-#endif
-constexpr int kNCW = PKV_DECODE_WARPS;   // consumer warps per CTA
-constexpr int kNST = PKV_DECODE_STAGES;  // shared-memory pipeline stages per CTA
+
+// Consumer warps and stages per CTA. The paged kernels stream: two consumer warps keep up
+// with HBM, and the shared memory goes to stages. The ring kernels rotate every key (RoPE on
+// read) and are bound by the consumers' arithmetic: four consumer warps, eight stages.
+constexpr int kNCW = PKV_DECODE_WARPS, kNST = PKV_DECODE_STAGES;
+constexpr int kNCWRing = 4, kNSTRing = 8;
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, DecodeArgs);
 
@@ -1070,17 +1082,20 @@ struct Variant {
   const void* fn;
   int mt;
   bool ring;
+  int threads;
+  size_t (*smem)(int R, int B, int newkv_bytes);
 };
+
+template <int NCW, int NST, int MT>
+size_t smem_of(int R, int B, int newkv_bytes) {
+  return Smem<NCW, NST, MT>::bytes(R, B, newkv_bytes);
+}
 
 template <int MT, bool RING, bool APPEND>
 Variant variant() {
-  return Variant{reinterpret_cast<const void*>(&decode_kernel<kNCW, kNST, MT, RING, APPEND>), MT,
-                 RING};
-}
-
-size_t smem_bytes(int mt, int R, int B, int newkv_bytes) {
-  return mt == 1 ? Smem<kNCW, kNST, 1>::bytes(R, B, newkv_bytes)
-                 : Smem<kNCW, kNST, 2>::bytes(R, B, newkv_bytes);
+  constexpr int NCW = RING ? kNCWRing : kNCW, NST = RING ? kNSTRing : kNST;
+  return Variant{reinterpret_cast<const void*>(&decode_kernel<NCW, NST, MT, RING, APPEND>), MT,
+                 RING, (NCW + 2) * 32, &smem_of<NCW, NST, MT>};
 }
 
 // Persistent grid for a variant: SM count x resident CTAs (capped), cached per device/size.
@@ -1104,7 +1119,7 @@ int grid_size(const Variant& v, size_t smem, int* status) {
     e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
   int occ = 0;
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, (kNCW + 2) * 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, v.threads, smem);
   if (e != cudaSuccess) { *status = cuda_status(e); return 0; }
   if (occ < 1) { *status = PKV_EINVAL; return 0; }
 #ifdef PKV_CTAS_PER_SM
@@ -1182,7 +1197,7 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   Variant v = ring     ? (mt == 1 ? variant<1, true, false>() : variant<2, true, false>())
               : append ? (mt == 1 ? variant<1, false, true>() : variant<2, false, true>())
                        : (mt == 1 ? variant<1, false, false>() : variant<2, false, false>());
-  const size_t smem = smem_bytes(mt, R, num_seqs, append ? 2 * q_len * 512 : 0);
+  const size_t smem = v.smem(R, num_seqs, append ? 2 * q_len * 512 : 0);
   if (smem > 227 * 1024) return PKV_EINVAL;
   int status = PKV_OK;
   const int grid = grid_size(v, smem, &status);
@@ -1238,7 +1253,7 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   void* params[4] = {&tmK, &tmV, &tmQ, &args};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3((kNCW + 2) * 32);
+  cfg.blockDim = dim3(v.threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   // the fused-append call may start while the preceding kernel finishes (see the kernel)
