@@ -388,7 +388,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
 // Warp roles: warps 0..NCW-1 consume chunks, warp NCW produces (TMA), warp NCW+1 is the
 // epilogue (merges each segment's per-warp states, writes outputs and split-unit partials,
 // announces arrivals), so the consumers never stop at a unit boundary.
-template <int NCW, int NST, int MT, bool RING, bool APPEND>
+template <int NCW, int NST, int MT, bool RING, bool APPEND, bool TR>
 __global__ void __launch_bounds__((NCW + 2) * 32, MT == 1 ? kMinCtasMt1 : 1)
 decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
@@ -399,6 +399,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   // last completed one (all that a parity wait can tell apart).
   static_assert(NST % NCW == 0, "pipeline stages must be a multiple of the consumer warps");
   static_assert(!(RING && APPEND), "the ring variant appends through its own slot mapping");
+  static_assert(!TR || (MT == 1 && !RING), "the transposed tile is for up to 8 rows, paged");
   // the queries' buffer stays in use for the whole segment when its fragments are not kept in
   // registers, or when it also holds the segment's new K/V rows
   constexpr bool kHoldQ = MT != 1 || APPEND;
@@ -713,6 +714,171 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         named_barrier_sync(1, kNC);   // consumers only
       }
 
+      if constexpr (TR) {
+      // ---- up to 8 rows: the transposed tile. S^T = K Q^T and O^T = V^T P^T, so the 16 keys
+      // of a chunk (and 16 dims of O) fill the mma's 16-row side and the (at most 8) query rows
+      // its 8 columns: half the mma of the 16-row form, half the accumulators. Thread (g, t4)
+      // holds rows 2t4 and 2t4 + 1 of the group, keys g and g + 8, dims 16 dt + g (+ 8).
+      // Q^T fragments (B operand): rows 0-7 of the query tile
+      uint32_t qb0[8], qb1[8];
+#pragma unroll
+      for (int s8 = 0; s8 < 8; ++s8) {
+        const int i = lane >> 3;
+        const int row = (i & 1) * 8 + (lane & 7);
+        const int ch = 2 * s8 + (i >> 1);
+        uint32_t unused0, unused1;
+        ldsm_x4(qb + (ch >> 3) * L::kQHalf + swz128(row, ch & 7), qb0[s8], unused0, qb1[s8],
+                unused1);
+      }
+      if (!kHoldQ) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
+      }
+      float tm[2] = {kNegInf, kNegInf}, tl[2] = {0.f, 0.f}, ot[8][4];
+#pragma unroll
+      for (int dt = 0; dt < 8; ++dt) ot[dt][0] = ot[dt][1] = ot[dt][2] = ot[dt][3] = 0.f;
+      int tlim[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int r = 2 * t4 + e;
+        const int qi = r < a.R ? r / a.G : a.q_len - 1;
+        tlim[e] = Lc - a.q_len + qi + 1;
+      }
+      const int nchunk = s.c1 - s.c0;
+      for (int jj = ((w - j) % NCW + NCW) % NCW; jj < nchunk; jj += NCW) {
+        const int gj = j + jj;
+        const int st = gj % NST;
+        if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
+        const uint32_t stK = sbase + st * kStageBytes;
+        const uint32_t stV = stK + 2 * kHalfBytes;
+        const int c = s.c0 + jj;
+        const bool full_chunk = (c + 1) * kChunk <= Lc - a.q_len + 1;
+        bool patched = false;
+        if (APPEND && (c + 1) * kChunk > Lc - a.q_len) {
+          const int first_new = Lc - a.q_len;
+          const int srow = srow_s[st];
+          const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
+          const int which = lane >> 4, ch = lane & 15;   // lanes 0-15: K, 16-31: V
+          for (int i = 0; i < a.q_len; ++i) {
+            const int pos = first_new + i;
+            if (pos < c * kChunk || pos >= (c + 1) * kChunk || pos < 0) continue;
+            const int tok = pos - c * kChunk;
+            const uint4 val = ld_shared_v4(nkv + i * 512 + which * 256 + ch * 16);
+            st_shared_v4((which ? stV : stK) + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), val);
+            if (srow >= 0) {
+              __half* pool = which ? a.v_pool : a.k_pool;
+              *reinterpret_cast<uint4*>(pool + (static_cast<int64_t>(srow) + tok) * kD + ch * 8) = val;
+            }
+          }
+          __syncwarp();
+          patched = true;
+        }
+        // ---- S^T = K Q^T: K fragments as the A operand (keys g, g + 8), two chains ----
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp) {
+          uint32_t k0[4], k1[4];   // keys 0-7 and 8-15, dims 32 sp .. 32 sp + 31
+          const int ch = 4 * sp + (lane >> 3);
+          ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(lane & 7, ch & 7), k0[0], k0[1], k0[2],
+                  k0[3]);
+          ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(8 + (lane & 7), ch & 7), k1[0], k1[1],
+                  k1[2], k1[3]);
+          // k-step 2 sp (dims 32 sp .. +15) and 2 sp + 1 (dims 32 sp + 16 .. +31)
+          mma_16816(sa, k0[0], k1[0], k0[1], k1[1], qb0[2 * sp], qb1[2 * sp]);
+          mma_16816(sb2, k0[2], k1[2], k0[3], k1[3], qb0[2 * sp + 1], qb1[2 * sp + 1]);
+        }
+        // ---- mask, online softmax over this thread's rows (exp2 domain) ----
+        // sa: [0] key g row 2t4, [1] key g row 2t4+1, [2] key g+8 row 2t4, [3] key g+8 row 2t4+1
+        float pv[4];
+        float alpha[2];
+        bool rescale = false;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int pos0 = c * kChunk + g, pos1 = pos0 + 8;
+          float x0 = (sa[e] + sb2[e]) * a.scale_log2;
+          float x1 = (sa[2 + e] + sb2[2 + e]) * a.scale_log2;
+          if (!full_chunk) {
+            x0 = pos0 < tlim[e] ? x0 : kNegInf;
+            x1 = pos1 < tlim[e] ? x1 : kNegInf;
+          }
+          float mx = fmaxf(x0, x1);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_old = tm[e];
+          const float m_new = fmaxf(m_old, mx);
+          const float m_use = m_new == kNegInf ? 0.f : m_new;
+          alpha[e] = fast_exp2(m_old - m_use);
+          rescale |= (m_old != kNegInf) && (m_new != m_old);
+          tm[e] = m_new;
+          pv[e] = fast_exp2(x0 - m_use);
+          pv[2 + e] = fast_exp2(x1 - m_use);
+          tl[e] = tl[e] * alpha[e] + (pv[e] + pv[2 + e]);
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int dt = 0; dt < 8; ++dt) {
+            ot[dt][0] *= alpha[0];
+            ot[dt][1] *= alpha[1];
+            ot[dt][2] *= alpha[0];
+            ot[dt][3] *= alpha[1];
+          }
+        }
+        // P^T (keys x rows) to the B operand (rows g, keys 2t4..): transpose the two 8x8 halves
+        const uint32_t pb0 = movmatrix_trans(pack_half2(pv[0], pv[1]));
+        const uint32_t pb1 = movmatrix_trans(pack_half2(pv[2], pv[3]));
+        // tokens no query may see may hold anything, NaN included: zero their V entries
+        uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+        if (!full_chunk) {
+          const int t0 = c * kChunk + 2 * t4;
+          vm0 = (t0 < Lc ? 0x0000ffffu : 0u) | (t0 + 1 < Lc ? 0xffff0000u : 0u);
+          vm1 = (t0 + 8 < Lc ? 0x0000ffffu : 0u) | (t0 + 9 < Lc ? 0xffff0000u : 0u);
+        }
+        // ---- O^T += V^T P^T: V fragments (ldmatrix.trans) as the A operand ----
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+          const int i = lane >> 3;
+          const int tok = (i & 1) * 8 + (lane & 7);
+          const int ch = 2 * dt + (i >> 1);
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_trans(stV + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), v0, v1, v2, v3);
+          v0 &= vm0; v1 &= vm1; v2 &= vm0; v3 &= vm1;
+          mma_16816(ot[dt], v0, v2, v1, v3, pb0, pb1);
+        }
+        if (APPEND && patched) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + st * 8);
+      }
+      if (kHoldQ) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
+      }
+      j += nchunk;
+      // ---- hand this warp's state to the epilogue: rows 2t4, 2t4 + 1 ----
+      const int sb = k & 1;
+      if (k >= 2 && !mbar_wait(bar_sfree + sb * 8, ((k >> 1) - 1) & 1, abort)) flag_timeout(a, abort);
+      float* o_d = stO + sb * NCW * a.R * kSt;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float lv = tl[e];
+        lv += __shfl_xor_sync(0xffffffffu, lv, 4);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+        const int r = 2 * t4 + e;
+        if (r < a.R) {
+          float* dst = o_d + (w * a.R + r) * kSt + g;
+#pragma unroll
+          for (int dt = 0; dt < 8; ++dt) {
+            dst[16 * dt] = ot[dt][e];
+            dst[16 * dt + 8] = ot[dt][2 + e];
+          }
+          if (g == 0) {
+            stM[(sb * NCW + w) * a.R + r] = tm[e];
+            stL[(sb * NCW + w) * a.R + r] = lv;
+          }
+        }
+      }
+      } else {
       // Q fragments (A operand, 16 rows x 128 dims per m-tile)
       uint32_t qf[MT == 1 ? 8 : 1][4];
       auto q_frag = [&](int mt, int s8, uint32_t (&f)[4]) {
@@ -990,8 +1156,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             }
           }
         }
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_sdone + sb * 8);
+      if (lane == 0) mbar_arrive(bar_sdone + (k & 1) * 8);
       ++k;
       has = cur.next(s);
     }
@@ -1091,11 +1258,11 @@ size_t smem_of(int R, int B, int newkv_bytes) {
   return Smem<NCW, NST, MT>::bytes(R, B, newkv_bytes);
 }
 
-template <int MT, bool RING, bool APPEND>
+template <int MT, bool RING, bool APPEND, bool TR = false>
 Variant variant() {
   constexpr int NCW = RING ? kNCWRing : kNCW, NST = RING ? kNSTRing : kNST;
-  return Variant{reinterpret_cast<const void*>(&decode_kernel<NCW, NST, MT, RING, APPEND>), MT,
-                 RING, (NCW + 2) * 32, &smem_of<NCW, NST, MT>};
+  return Variant{reinterpret_cast<const void*>(&decode_kernel<NCW, NST, MT, RING, APPEND, TR>),
+                 MT, RING, (NCW + 2) * 32, &smem_of<NCW, NST, MT>};
 }
 
 // Persistent grid for a variant: SM count x resident CTAs (capped), cached per device/size.
@@ -1194,9 +1361,13 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   if (workspace_bytes < ws.total) return PKV_ENOSPC;
 
   const int mt = R <= 16 ? 1 : 2;
+  // up to 8 rows per unit (GQA groups of 6-8 at one query token): the transposed tile
+  const bool tr = !ring && R <= 8;
   Variant v = ring     ? (mt == 1 ? variant<1, true, false>() : variant<2, true, false>())
-              : append ? (mt == 1 ? variant<1, false, true>() : variant<2, false, true>())
-                       : (mt == 1 ? variant<1, false, false>() : variant<2, false, false>());
+              : append ? (tr ? variant<1, false, true, true>()
+                             : mt == 1 ? variant<1, false, true>() : variant<2, false, true>())
+                       : (tr ? variant<1, false, false, true>()
+                             : mt == 1 ? variant<1, false, false>() : variant<2, false, false>());
   const size_t smem = v.smem(R, num_seqs, append ? 2 * q_len * 512 : 0);
   if (smem > 227 * 1024) return PKV_EINVAL;
   int status = PKV_OK;

@@ -142,6 +142,14 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
 }
 
 // D = A(16x16, row) * B(16x8, col) + D, f16 inputs, f32 accumulators.
+// Transpose of an 8x8 matrix of 16-bit elements held one pair per thread (thread t: row t/4,
+// columns 2(t%4), 2(t%4)+1) into the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
