@@ -8,24 +8,32 @@
 //
 // Design (GB300):
 //  * Work unit = (sequence b, kv head h). Every query head of the GQA group of h and every
-//    query token of b forms one row of a 16-row tile (R = G * q_len rows, padded to 16 or 32),
-//    so each K/V byte is read from HBM once for the whole group.
+//    query token of b forms one row of the unit's query tile (R = G * q_len rows), so each
+//    K/V byte is read from HBM once for the whole group.
 //  * The unit's context is cut into 16-token chunks (one chunk = 4 KB of K + 4 KB of V; a
-//    block of bs tokens is bs/16 consecutive chunks). All units' chunks form one stream, and
-//    every CTA of a persistent grid (SM count x resident CTAs) takes an equal contiguous
-//    slice of it: no CTA waits on a long sequence while others idle. A unit cut by slice
-//    boundaries leaves normalised partials (m, l, o) in the workspace; the CTA that arrives
-//    last on the unit's counter merges them in slice order (no spinning; the merge order and
-//    hence the result are independent of scheduling and of which physical blocks are used).
+//    block of bs tokens is bs/16 consecutive chunks). All units' chunks form one stream, in
+//    which every unit is preceded by kSegCost empty positions (the cost of a segment in chunk
+//    equivalents), and every CTA of a persistent grid (SM count x resident CTAs) takes an equal
+//    contiguous slice of it: no CTA waits on a long sequence while others idle. A unit cut by
+//    slice boundaries leaves normalised partials (m, l, o) in the workspace; the CTA holding
+//    its first chunk merges them in slice order once the others have announced theirs (a
+//    bounded wait; past it the last CTA to arrive merges instead, with the same partials in
+//    the same order), so the result does not depend on scheduling or on which physical
+//    blocks are used.
 //  * One producer warp walks the slice, stages the block-table entries in registers (one
 //    coalesced 32-entry load per 32 chunks: the block table never sits in the consumers'
 //    path) and issues TMA tile loads (128-byte swizzle) of K and V into an NST-deep ring of
 //    shared-memory stages, completing on mbarriers. The next chunks are in flight while the
 //    consumers work on the current one.
 //  * NCW consumer warps take the slice's chunks round-robin, each with its own online-softmax
-//    state: S = Q K^T with mma.sync m16n8k16 (f16 in, f32 accumulate; K fragments by ldmatrix
-//    from the swizzled tile), softmax in the exp2 domain, O += P V with V fragments by
-//    ldmatrix.trans. At each unit boundary the warps merge through shared memory.
+//    state; an epilogue warp merges their states at each unit boundary and writes the output
+//    or the partial. Scores and output come from mma.sync m16n8k16 (f16 in, f32 accumulate)
+//    on ldmatrix fragments of the swizzled tiles: for up to 8 rows as S^T = K Q^T and
+//    O^T = V^T P^T (keys and output dims on the mma's 16-row side), else as S = Q K^T and
+//    O = P V with the rows padded to 16 or 32. Softmax runs in the exp2 domain.
+//  * The fused-append launch may start while its predecessor finishes (programmatic
+//    dependent launch): it requests its first stages, then waits for the predecessor before
+//    touching queries, new K/V rows, outputs and the workspace.
 //  * No wait is unbounded: an mbarrier wait gives up after kWaitLimit polls, sets
 //    PKV_DEVERR_TIMEOUT and lets the kernel finish. Out-of-range block ids become
 //    out-of-bounds TMA boxes (zero fill) and set PKV_DEVERR_BLOCK_ID.
@@ -296,8 +304,9 @@ struct MergeStage {
   }
 };
 
-// Merge of a split unit's partials, run cooperatively by NT threads of the last CTA to arrive
-// on the unit's counter, after its whole slice is done (so its pipeline stages are free).
+// Merge of a split unit's partials, run cooperatively by NT threads of the merging CTA (the one
+// holding the unit's first chunk, or the last to arrive on the unit's counter), after its whole
+// slice is done (so its pipeline stages are free).
 // Partial p (in slice order) holds per row its max m_p, sum l_p and normalised output o_p; the
 // result is sum_p o_p l_p 2^(m_p - M) / sum_p l_p 2^(m_p - M), M = max_p m_p, formed in slice
 // order. The partials are copied into the stage memory with cp.async (as many per batch as fit,
