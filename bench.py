@@ -203,6 +203,14 @@ class Step:
                                            self.k[l], self.v[l], self.bt, self.cl, w.scale,
                                            self.ws)
 
+    def run_append_only(self):
+        """The standalone KV append of the step (slot mapping once, then one append per
+        layer): what the fused call replaces, timed for comparison."""
+        p, w = self.pkv, self.w
+        p.slot_mapping(self.seq, self.pos, self.bt, w.block_size, out=self.slots)
+        for l in range(w.num_layers):
+            p.kv_append(self.kn[l], self.vn[l], self.slots, self.k[l], self.v[l])
+
     def run_decode_only(self):
         p, w = self.pkv, self.w
         if self.kind == "ring":
@@ -307,6 +315,10 @@ def run_ours(args, w, rank, local_rank, world_size):
     traffic = traffic_record(w)
     dsteps = max(10, args.steps // 2)
     plain_per_launch = time_replays(decode_graph, dsteps, args.warmup) / (dsteps * w.num_layers)
+    append_per_launch = None
+    if st.kind == "fused":
+        append_graph = capture(st.run_append_only)
+        append_per_launch = time_replays(append_graph, dsteps, args.warmup) / (dsteps * w.num_layers)
 
     e2e = None
     if not args.no_e2e:
@@ -360,6 +372,8 @@ def run_ours(args, w, rank, local_rank, world_size):
                      "kernel": st.kernel_note(),
                      "launch_us": round(per_launch * 1e6, 3),
                      "unfused_decode_launch_us": round(plain_per_launch * 1e6, 3),
+                     "standalone_kv_append_launch_us":
+                         None if append_per_launch is None else round(append_per_launch * 1e6, 3),
                      "algorithmic_bytes_per_launch": int(bytes_launch),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": e2e,
