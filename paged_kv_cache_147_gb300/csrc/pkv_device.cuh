@@ -200,7 +200,6 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   return v;
 }
 
-__device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
 
 // 16-byte global -> shared copy that bypasses L1 (Ampere-style cp.async), and its wait.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
