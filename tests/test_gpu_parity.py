@@ -274,6 +274,9 @@ def _gpu_decode(k, v, tables, lens, q, scale, bs=16):
     ([1000, 3, 517], 64, 32, 32, 1),                       # MHA, 64-token blocks
     ([300, 47], 16, 64, 8, 1),                             # GQA 8
     ([77, 200, 5], 16, 12, 2, 3),                          # causal multi-query (R = 18)
+    ([77, 200, 5], 16, 8, 4, 4),                           # causal, transposed tile (R = 8)
+    ([33, 1, 60], 16, 4, 4, 3),                            # MHA drafts (R = 3)
+    ([500, 70], 64, 16, 2, 1),                             # GQA 8, 64-token blocks
     ([129, 64], 32, 64, 8, 4),                             # R = 32, 32-token blocks
     ([20000], 16, 12, 2, 1),                               # one long sequence over many CTAs
     ([5] * 700, 16, 12, 2, 1),                             # many short sequences
