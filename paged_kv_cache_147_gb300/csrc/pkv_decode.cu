@@ -516,6 +516,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   if (warp == NCW) {
     // =================================== producer ============================================
     const int chunk_mask = (1 << a.bs_shift) - 1;
+    const uint64_t kv_policy = l2_policy_evict_first();
     int j = 0, k = 0;
     Seg s;
     bool has = cur.first(begin, s);
@@ -596,10 +597,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (APPEND) srow_s[st] = r;   // published to the consumer by the barrier below
             mbar_arrive_expect_tx(fb, kStageBytes);
             const uint32_t dst = sbase + st * kStageBytes;
-            tma_load_2d(dst, &tmK, 0, r, fb);
-            tma_load_2d(dst + kHalfBytes, &tmK, 64, r, fb);
-            tma_load_2d(dst + 2 * kHalfBytes, &tmV, 0, r, fb);
-            tma_load_2d(dst + 3 * kHalfBytes, &tmV, 64, r, fb);
+            // K/V are read once per step: first to go from L2, which then keeps the
+            // partials, queries and tables the merges and other CTAs need
+            tma_load_2d_hint(dst, &tmK, 0, r, fb, kv_policy);
+            tma_load_2d_hint(dst + kHalfBytes, &tmK, 64, r, fb, kv_policy);
+            tma_load_2d_hint(dst + 2 * kHalfBytes, &tmV, 0, r, fb, kv_policy);
+            tma_load_2d_hint(dst + 3 * kHalfBytes, &tmV, 64, r, fb, kv_policy);
           }
         }
       }
