@@ -120,6 +120,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 template <int NCW, int NST, int MT>
 struct Smem {
+  static constexpr int kNST = NST;
   static constexpr int kQHalf = MT * 2048;            // 16*MT rows x 128 B
   static constexpr int kQBuf = 2 * kQHalf;
   static constexpr int kQ = NST * kStageBytes;
@@ -393,6 +394,32 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
   merge_sync<NT>();                        // stage memory free for the next merge
 }
 
+// Requests segment kk's queries (and, fused append, its new K/V rows) into query buffer kk & 1,
+// completing on that buffer's full barrier; waits first until the consumers have released the
+// buffer's previous use. One thread.
+template <class L, bool APPEND>
+__device__ __forceinline__ void issue_queries(const DecodeArgs& a, const CUtensorMap* tmQ,
+                                              uint32_t sbase, int B, const Seg& sg, int kk,
+                                              volatile int* abort) {
+  const uint32_t bar_qfull = sbase + L::kBars + 2 * L::kNST * 8;
+  const uint32_t bar_qempty = bar_qfull + 2 * 8;
+  const int qs = kk & 1;
+  if (kk >= 2 && !mbar_wait(bar_qempty + qs * 8, ((kk >> 1) - 1) & 1, abort))
+    flag_timeout(a, abort);
+  mbar_arrive_expect_tx(bar_qfull + qs * 8, a.R * 256 + (APPEND ? a.q_len * 512 : 0));
+  const uint32_t qdst = sbase + L::kQ + qs * L::kQBuf;
+  tma_load_3d(qdst, tmQ, 0, sg.h * a.G, sg.b * a.q_len, bar_qfull + qs * 8);
+  tma_load_3d(qdst + L::kQHalf, tmQ, 64, sg.h * a.G, sg.b * a.q_len, bar_qfull + qs * 8);
+  if (APPEND) {
+    const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
+    for (int i = 0; i < a.q_len; ++i) {
+      const int64_t row = (static_cast<int64_t>(sg.b) * a.q_len + i) * a.Hkv + sg.h;
+      bulk_load(nkv + i * 512, a.k_new + row * kD, 256, bar_qfull + qs * 8);
+      bulk_load(nkv + i * 512 + 256, a.v_new + row * kD, 256, bar_qfull + qs * 8);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 // Warp roles: warps 0..NCW-1 consume chunks, warp NCW produces (TMA), warp NCW+1 is the
 // epilogue (merges each segment's per-warp states, writes outputs and split-unit partials,
@@ -541,27 +568,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     // as they are never launched early).
     const bool early_kv = APPEND;
     bool waited = false;
-    const Seg first_seg = s;
     auto issue_q = [&](const Seg& sg, int kk) {
-      if (lane != 0) return;
-      const int qs = kk & 1;
-      if (kk >= 2 && !mbar_wait(bar_qempty + qs * 8, ((kk >> 1) - 1) & 1, abort))
-        flag_timeout(a, abort);
-      mbar_arrive_expect_tx(bar_qfull + qs * 8, a.R * 256 + (APPEND ? a.q_len * 512 : 0));
-      const uint32_t qdst = sbase + L::kQ + qs * L::kQBuf;
-      tma_load_3d(qdst, &tmQ, 0, sg.h * a.G, sg.b * a.q_len, bar_qfull + qs * 8);
-      tma_load_3d(qdst + L::kQHalf, &tmQ, 64, sg.h * a.G, sg.b * a.q_len, bar_qfull + qs * 8);
-      if (APPEND) {
-        const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
-        for (int i = 0; i < a.q_len; ++i) {
-          const int64_t row = (static_cast<int64_t>(sg.b) * a.q_len + i) * a.Hkv + sg.h;
-          bulk_load(nkv + i * 512, a.k_new + row * kD, 256, bar_qfull + qs * 8);
-          bulk_load(nkv + i * 512 + 256, a.v_new + row * kD, 256, bar_qfull + qs * 8);
-        }
-      }
+      if (lane == 0) issue_queries<L, APPEND>(a, &tmQ, sbase, B, sg, kk, abort);
     };
     while (has) {
-      if (!early_kv || waited) {
+      // with an early start the epilogue warp requests the first segment's queries (it is
+      // idle until a segment ends): they go out as soon as the dependency is met, while
+      // this warp is still filling the stages
+      if (!early_kv || k > 0) {
         if (!waited) { griddep_wait(); waited = true; }
         issue_q(s, k);
       }
@@ -583,10 +597,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const int n = min(32, s.c1 - cb);
         for (int l = 0; l < n; ++l, ++j) {
           if (early_kv && !waited && j == NST) {
-            // every stage is requested; the consumers need the first queries to free one
+            // every stage is requested; none frees before the dependency is met
             griddep_wait();
             waited = true;
-            issue_q(first_seg, 0);
           }
           const int r = __shfl_sync(0xffffffffu, row, l);
           if (lane == 0) {
@@ -605,12 +618,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             tma_load_2d_hint(dst + 3 * kHalfBytes, &tmV, 64, r, fb, kv_policy);
           }
         }
-      }
-      if (early_kv && !waited) {
-        // the first segment ended before the stages filled: its queries come now
-        griddep_wait();
-        waited = true;
-        issue_q(first_seg, 0);
       }
       ++k;
       s = nx;
@@ -660,6 +667,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     int k = 0, npend = 0;
     Seg s;
     bool has = cur.first(begin, s);
+    if (APPEND && has) {
+      griddep_wait();
+      if (lane == 0) issue_queries<L, APPEND>(a, &tmQ, sbase, B, s, 0, abort);
+    }
     while (has && k < last_k) {
       const int sb = k & 1;
       if (!mbar_wait(bar_sdone + sb * 8, (k >> 1) & 1, abort)) flag_timeout(a, abort);
