@@ -289,6 +289,41 @@ __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const float* 
   }
 }
 
+// The same merge of a segment's per-warp states by NT > 32 threads (the CTA's last segment, at
+// the end of the launch): one thread per row forms the row's weights once and leaves them in
+// the row's padding (floats kD.. of each state row), then every thread sums its own 4 dims.
+template <int NCW, int NT>
+__device__ __forceinline__ void merge_segment_wide(const DecodeArgs& a, float* o_s,
+                                                   const float* m_s, const float* l_s, int b,
+                                                   int h, bool complete, float* po, float* pml,
+                                                   int t) {
+  const int R = a.R;
+  if (t < R) {
+    float w[NCW], row_m, row_l;
+    row_weights<NCW>(m_s, l_s, R, t, w, row_m, row_l);
+#pragma unroll
+    for (int ww = 0; ww < NCW; ++ww) o_s[(ww * R + t) * kSt + kD] = w[ww];
+    if (!complete) *reinterpret_cast<float4*>(pml + t * 4) = make_float4(row_m, row_l, 0.f, 0.f);
+  }
+  named_barrier_sync(2, NT);
+#pragma unroll 1
+  for (int gi = t; gi < R * 32; gi += NT) {
+    const int r = gi >> 5, c4 = gi & 31;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int ww = 0; ww < NCW; ++ww) {
+      const float* row = o_s + (ww * R + r) * kSt;
+      const float4 v = reinterpret_cast<const float4*>(row)[c4];
+      const float wt = row[kD];
+      acc.x += wt * v.x; acc.y += wt * v.y; acc.z += wt * v.z; acc.w += wt * v.w;
+    }
+    if (complete)
+      store_half4(out_row(a, b, h, r) + c4 * 4, acc);
+    else
+      reinterpret_cast<float4*>(po + r * kD)[c4] = acc;
+  }
+}
+
 // Where merge_unit stages partials in the (free) pipeline stage memory.
 struct MergeStage {
   float* accv;    // [R][128] running output
@@ -309,10 +344,12 @@ struct MergeStage {
 // holding the unit's first chunk, or the last to arrive on the unit's counter), after its whole
 // slice is done (so its pipeline stages are free).
 // Partial p (in slice order) holds per row its max m_p, sum l_p and normalised output o_p; the
-// result is sum_p o_p l_p 2^(m_p - M) / sum_p l_p 2^(m_p - M), M = max_p m_p, formed in slice
+// result is sum_p o_p w_p / sum_p w_p with w_p = l_p 2^(m_p - M), M = max_p m_p, formed in slice
 // order. The partials are copied into the stage memory with cp.async (as many per batch as fit,
-// usually all: one round trip to L2); each thread then reduces its own 4 output dims in one
-// pass, recomputing its row's weights, with no barrier inside a batch.
+// usually all: one round trip to L2); then one thread per row forms the row's weights (already
+// divided by the row's sum in the last batch), and every thread sums its own 4 output dims over
+// the partials. Each pass is short and independent across threads: this runs once per CTA at
+// the end of the launch, where its latency is on the critical path.
 // own >= 0: the unit's first partial (own == cf, the merging CTA's own) is already in the
 // staging area, at index 0 of the first batch; it is not copied from the workspace.
 template <int NT>
@@ -330,7 +367,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
   float* rowml = ms.rowml;
   const int PB = ms.PB;
   float* so = ms.so;
-  float* sml = ms.sml;
+  float* sml = ms.sml;   // per partial and row: m, l, then this batch's weight and row scale
   const uint32_t so_s = smem_u32(so), sml_s = smem_u32(sml);
   const int o_vec = R * kD / 4;                            // 16-byte pieces of one partial's o
   int batch = 0;
@@ -339,55 +376,64 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
     const int nbp = min(PB, cl - base + 1);
     const bool last_batch = base + PB > cl;
     merge_sync<NT>();                      // previous batch fully used
-#pragma unroll 4
-    for (int i = t; i < nbp * (o_vec + R); i += NT) {
-      const bool is_o = i < nbp * o_vec;
-      const int j = is_o ? i : i - nbp * o_vec;
-      const int per_part = is_o ? o_vec : R;
-      const int p = j / per_part, off = j - p * per_part;
+#pragma unroll 1
+    for (int p = 0; p < nbp; ++p) {
       const int cc = base + p;
       if (cc == own) continue;
       const int64_t sl = 2 * cc + ((cc == cf && first_odd) ? 1 : 0);
-      if (is_o)
-        cp_async_16(so_s + (p * R * kD + off * 4) * 4, a.part_o + sl * R * kD + off * 4);
-      else
-        cp_async_16(sml_s + (p * R + off) * 16, a.part_ml + (sl * R + off) * 4);
+      const float* src = a.part_o + sl * R * kD;
+      const uint32_t dst = so_s + p * R * kD * 4;
+      for (int i = t; i < o_vec; i += NT) cp_async_16(dst + i * 16, src + i * 4);
+      if (t < R) cp_async_16(sml_s + (p * R + t) * 16, a.part_ml + (sl * R + t) * 4);
     }
     cp_async_wait_all();
     merge_sync<NT>();
-    const float* rin = rowml + (batch & 1) * 2 * R;
-    float* rout = rowml + ((batch + 1) & 1) * 2 * R;
+    if (t < R) {
+      const float* rin = rowml + (batch & 1) * 2 * R;
+      float* rout = rowml + ((batch + 1) & 1) * 2 * R;
+      const float M0 = batch ? rin[2 * t] : kNegInf;
+      const float L0 = batch ? rin[2 * t + 1] : 0.f;
+      float M = M0;
+#pragma unroll 4
+      for (int p = 0; p < nbp; ++p) M = fmaxf(M, sml[(p * R + t) * 4]);
+      const float sc = (M0 == kNegInf || M == kNegInf) ? 0.f : fast_exp2(M0 - M);
+      float L = L0 * sc;
+#pragma unroll 4
+      for (int p = 0; p < nbp; ++p) {
+        float* e = sml + (p * R + t) * 4;
+        const float wp = e[0] == kNegInf ? 0.f : e[1] * fast_exp2(e[0] - M);
+        L += wp;
+        e[2] = wp;
+      }
+      const float inv = !last_batch ? 1.f : (L > 0.f ? 1.f / L : 0.f);
+      if (last_batch) {
+#pragma unroll 4
+        for (int p = 0; p < nbp; ++p) sml[(p * R + t) * 4 + 2] *= inv;
+      }
+      sml[t * 4 + 3] = sc * inv;           // scale of the running sum from earlier batches
+      rout[2 * t] = M;
+      rout[2 * t + 1] = L;
+    }
+    merge_sync<NT>();
 #pragma unroll 1
     for (int gi = t; gi < R * 32; gi += NT) {
       const int r = gi >> 5, c4 = gi & 31;
-      const float M0 = batch ? rin[2 * r] : kNegInf;
-      const float L0 = batch ? rin[2 * r + 1] : 0.f;
-      float M = M0;
-#pragma unroll 4
-      for (int p = 0; p < nbp; ++p) M = fmaxf(M, sml[(p * R + r) * 4]);
-      const float sc = (M0 == kNegInf || M == kNegInf) ? 0.f : fast_exp2(M0 - M);
-      float L = L0 * sc;
       float4 V = make_float4(0.f, 0.f, 0.f, 0.f);
       if (batch) {
+        const float sc = sml[r * 4 + 3];
         V = reinterpret_cast<const float4*>(accv)[gi];
         V.x *= sc; V.y *= sc; V.z *= sc; V.w *= sc;
       }
 #pragma unroll 4
       for (int p = 0; p < nbp; ++p) {
-        const float2 ml = *reinterpret_cast<const float2*>(sml + (p * R + r) * 4);
-        const float wp = ml.x == kNegInf ? 0.f : ml.y * fast_exp2(ml.x - M);
+        const float wp = sml[(p * R + r) * 4 + 2];
         const float4 o4 = reinterpret_cast<const float4*>(so + (p * R + r) * kD)[c4];
-        L += wp;
         V.x += wp * o4.x; V.y += wp * o4.y; V.z += wp * o4.z; V.w += wp * o4.w;
       }
-      if (last_batch) {
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        V.x *= inv; V.y *= inv; V.z *= inv; V.w *= inv;
+      if (last_batch)
         store_half4(out_row(a, b, h, r) + c4 * 4, V);
-      } else {
+      else
         reinterpret_cast<float4*>(accv)[gi] = V;
-        if (c4 == 0) { rout[2 * r] = M; rout[2 * r + 1] = L; }
-      }
     }
   }
   if (t == 0) a.counters[b * a.Hkv + h] = 0;
@@ -1196,7 +1242,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const MergeStage ms(smem, NST * kStageBytes, a.R);
     named_barrier_sync(2, kNE);                  // last states written, earlier segments merged
     const int sb = last_k & 1;
-    const float* so_w = stO + sb * NCW * a.R * kSt;
+    float* so_w = stO + sb * NCW * a.R * kSt;
     const float* sm_w = stM + sb * NCW * a.R;
     const float* sl_w = stL + sb * NCW * a.R;
     int* counter = a.counters + last_b * a.Hkv + last_h;
@@ -1210,7 +1256,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     // partials and their order are the same, so the result does not depend on the path.
     bool merged = false;
     if (!last_complete && last_head) {
-      merge_segment<NCW, kNE>(a, so_w, sm_w, sl_w, last_b, last_h, false, ms.so, ms.sml, t);
+      merge_segment_wide<NCW, kNE>(a, so_w, sm_w, sl_w, last_b, last_h, false, ms.so, ms.sml,
+                                   t);
       if (t == 0) {
         const uint64_t t_end = global_time_ns() + kMergeWaitNs;
         int ok = 0;
@@ -1233,9 +1280,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         if (t < a.R) reinterpret_cast<float4*>(pml)[t] = reinterpret_cast<const float4*>(ms.sml)[t];
       }
     } else {
-      merge_segment<NCW, kNE>(a, so_w, sm_w, sl_w, last_b, last_h, last_complete,
-                              a.part_o + static_cast<int64_t>(last_slot) * a.R * kD,
-                              a.part_ml + static_cast<int64_t>(last_slot) * a.R * 4, t);
+      merge_segment_wide<NCW, kNE>(a, so_w, sm_w, sl_w, last_b, last_h, last_complete,
+                                   a.part_o + static_cast<int64_t>(last_slot) * a.R * kD,
+                                   a.part_ml + static_cast<int64_t>(last_slot) * a.R * 4, t);
     }
     if (!last_complete && !merged) {
       named_barrier_sync(2, kNE);                // partial written by every thread
