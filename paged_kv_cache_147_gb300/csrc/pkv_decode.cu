@@ -327,15 +327,16 @@ __device__ __forceinline__ void merge_segment_wide(const DecodeArgs& a, float* o
 // Where merge_unit stages partials in the (free) pipeline stage memory.
 struct MergeStage {
   float* accv;    // [R][128] running output
-  float* rowml;   // [2][R][2] running (max, sum)
+  float* rowml;   // [2][R][2] running (max, sum), then [R][2] (scale of the running output,
+                  // 1 / sum in the last batch) and [R][2] spare (keeps `so` 16-byte aligned)
   float* so;      // [PB][R][128] partials' o
-  float* sml;     // [PB][R][4] partials' (m, l, -, -)
+  float* sml;     // [PB][R][4] partials' (m, l, weight, -)
   int PB;         // partials per batch (>= 2)
   __device__ MergeStage(uint8_t* stage_mem, int stage_bytes, int R) {
     accv = reinterpret_cast<float*>(stage_mem);
     rowml = accv + R * kD;
-    PB = (stage_bytes - (R * kD + 4 * R) * 4) / (R * (kD + 4) * 4);
-    so = rowml + 4 * R;
+    PB = (stage_bytes - (R * kD + 8 * R) * 4) / (R * (kD + 4) * 4);
+    so = rowml + 8 * R;
     sml = so + PB * R * kD;
   }
 };
@@ -346,10 +347,10 @@ struct MergeStage {
 // Partial p (in slice order) holds per row its max m_p, sum l_p and normalised output o_p; the
 // result is sum_p o_p w_p / sum_p w_p with w_p = l_p 2^(m_p - M), M = max_p m_p, formed in slice
 // order. The partials are copied into the stage memory with cp.async (as many per batch as fit,
-// usually all: one round trip to L2); then one thread per row forms the row's weights (already
-// divided by the row's sum in the last batch), and every thread sums its own 4 output dims over
-// the partials. Each pass is short and independent across threads: this runs once per CTA at
-// the end of the launch, where its latency is on the critical path.
+// usually all: one round trip to L2); then one thread per row forms the row's weights, and every
+// thread sums its own 4 output dims over the partials and divides by the row's sum. Each pass
+// takes few dependent shared-memory round trips: this runs once per CTA at the end of the
+// launch, where its latency is on the critical path.
 // own >= 0: the unit's first partial (own == cf, the merging CTA's own) is already in the
 // staging area, at index 0 of the first batch; it is not copied from the workspace.
 template <int NT>
@@ -367,7 +368,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
   float* rowml = ms.rowml;
   const int PB = ms.PB;
   float* so = ms.so;
-  float* sml = ms.sml;   // per partial and row: m, l, then this batch's weight and row scale
+  float* sml = ms.sml;   // per partial and row: m, l, then this batch's weight
   const uint32_t so_s = smem_u32(so), sml_s = smem_u32(sml);
   const int o_vec = R * kD / 4;                            // 16-byte pieces of one partial's o
   int batch = 0;
@@ -388,29 +389,50 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
     }
     cp_async_wait_all();
     merge_sync<NT>();
+    float* rsc = rowml + 4 * R;
     if (t < R) {
+      // The row's (m, l) pairs are read into registers kRegP at a time (one shared-memory round
+      // trip per group; a single one in the usual case of at most kRegP partials) before any
+      // weight is written back.
+      constexpr int kRegP = 8;
       const float* rin = rowml + (batch & 1) * 2 * R;
       float* rout = rowml + ((batch + 1) & 1) * 2 * R;
       const float M0 = batch ? rin[2 * t] : kNegInf;
       const float L0 = batch ? rin[2 * t + 1] : 0.f;
+      float2 mlr[kRegP];
       float M = M0;
-#pragma unroll 4
-      for (int p = 0; p < nbp; ++p) M = fmaxf(M, sml[(p * R + t) * 4]);
+#pragma unroll 1
+      for (int p0 = 0; p0 < nbp; p0 += kRegP) {
+#pragma unroll
+        for (int i = 0; i < kRegP; ++i) {
+          const int p = p0 + i;
+          mlr[i] = p < nbp ? *reinterpret_cast<const float2*>(sml + (p * R + t) * 4)
+                           : make_float2(kNegInf, 0.f);
+          M = fmaxf(M, mlr[i].x);
+        }
+      }
       const float sc = (M0 == kNegInf || M == kNegInf) ? 0.f : fast_exp2(M0 - M);
       float L = L0 * sc;
-#pragma unroll 4
-      for (int p = 0; p < nbp; ++p) {
-        float* e = sml + (p * R + t) * 4;
-        const float wp = e[0] == kNegInf ? 0.f : e[1] * fast_exp2(e[0] - M);
-        L += wp;
-        e[2] = wp;
+#pragma unroll 1
+      for (int p0 = 0; p0 < nbp; p0 += kRegP) {
+        if (nbp > kRegP) {
+#pragma unroll
+          for (int i = 0; i < kRegP; ++i) {
+            const int p = p0 + i;
+            mlr[i] = p < nbp ? *reinterpret_cast<const float2*>(sml + (p * R + t) * 4)
+                             : make_float2(kNegInf, 0.f);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kRegP; ++i) {
+          const int p = p0 + i;
+          const float wp = mlr[i].x == kNegInf ? 0.f : mlr[i].y * fast_exp2(mlr[i].x - M);
+          L += wp;
+          if (p < nbp) sml[(p * R + t) * 4 + 2] = wp;
+        }
       }
       const float inv = !last_batch ? 1.f : (L > 0.f ? 1.f / L : 0.f);
-      if (last_batch) {
-#pragma unroll 4
-        for (int p = 0; p < nbp; ++p) sml[(p * R + t) * 4 + 2] *= inv;
-      }
-      sml[t * 4 + 3] = sc * inv;           // scale of the running sum from earlier batches
+      *reinterpret_cast<float2*>(rsc + 2 * t) = make_float2(sc, inv);
       rout[2 * t] = M;
       rout[2 * t + 1] = L;
     }
@@ -418,11 +440,11 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
 #pragma unroll 1
     for (int gi = t; gi < R * 32; gi += NT) {
       const int r = gi >> 5, c4 = gi & 31;
+      const float2 si = *reinterpret_cast<const float2*>(rsc + 2 * r);
       float4 V = make_float4(0.f, 0.f, 0.f, 0.f);
       if (batch) {
-        const float sc = sml[r * 4 + 3];
         V = reinterpret_cast<const float4*>(accv)[gi];
-        V.x *= sc; V.y *= sc; V.z *= sc; V.w *= sc;
+        V.x *= si.x; V.y *= si.x; V.z *= si.x; V.w *= si.x;
       }
 #pragma unroll 4
       for (int p = 0; p < nbp; ++p) {
@@ -430,10 +452,12 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
         const float4 o4 = reinterpret_cast<const float4*>(so + (p * R + r) * kD)[c4];
         V.x += wp * o4.x; V.y += wp * o4.y; V.z += wp * o4.z; V.w += wp * o4.w;
       }
-      if (last_batch)
+      if (last_batch) {
+        V.x *= si.y; V.y *= si.y; V.z *= si.y; V.w *= si.y;
         store_half4(out_row(a, b, h, r) + c4 * 4, V);
-      else
+      } else {
         reinterpret_cast<float4*>(accv)[gi] = V;
+      }
     }
   }
   if (t == 0) a.counters[b * a.Hkv + h] = 0;
