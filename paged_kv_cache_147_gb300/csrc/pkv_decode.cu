@@ -1383,11 +1383,7 @@ int grid_size(const Variant& v, size_t smem, int* status) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, v.threads, smem);
   if (e != cudaSuccess) { *status = cuda_status(e); return 0; }
   if (occ < 1) { *status = PKV_EINVAL; return 0; }
-#ifdef PKV_CTAS_PER_SM
-  const int grid = sm_count() * std::min(std::min(occ, kMaxCtasPerSm), PKV_CTAS_PER_SM);
-#else
   const int grid = sm_count() * std::min(occ, kMaxCtasPerSm);
-#endif
   cache[key] = grid;
   return grid;
 }
