@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the CPU-baseline sample")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="fewer layers than the workload's (small profiler captures; the "
+                         "per-launch figures are unchanged, the step and the L2 note shrink)")
     return ap.parse_args()
 
 
@@ -101,8 +104,10 @@ def describe(w) -> dict:
         "context_min_mean_max": [int(cl.min()), round(float(cl.mean()), 1), int(cl.max())],
         "kv_bytes_per_step": nbytes,
         "accumulate": "f32",
-        "l2": f"no flush: one step reads {nbytes / 1e9:.2f} GB of K/V, "
-              f"more than the {L2_BYTES / 2**20:.0f} MiB L2",
+        "l2": (f"no flush: one step reads {nbytes / 1e9:.2f} GB of K/V, "
+               f"more than the {L2_BYTES / 2**20:.0f} MiB L2") if nbytes > L2_BYTES else
+              (f"no flush and a step of {nbytes / 1e6:.1f} MB of K/V, within the "
+               f"{L2_BYTES / 2**20:.0f} MiB L2: not an HBM measurement"),
     }
 
 
@@ -538,6 +543,8 @@ def main():
     # the ring cache spans 24 layers of the 1.1B shape, so that a step exceeds L2
     w = workloads.ring(num_layers=24) if args.workload == "ring" else \
         workloads.WORKLOADS[args.workload]()
+    if args.layers is not None:
+        w.num_layers = max(1, min(args.layers, w.num_layers))
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w, world_size)), flush=True)
