@@ -9,6 +9,10 @@ page passage it restates); this module loads it with ctypes, building it with th
 compiler when the shared object is missing or older than its source. fp16 arrays cross the
 boundary as their raw ``uint16`` bit patterns.
 
+The FP8 (E4M3) cache functions are pinned against torch's float8_e4m3fn decoding and rounding,
+the format's landmark values, a brute-force nearest search and the fp16 oracle on an exactly
+representable cache.
+
 Parity status: pinned by the CPU tests, except the ring valid-set rule after a rollback, a
 reading of the streaming page that the pages themselves do not fix (parity unpinned against
 the pages there; pinned only by an independent linear-history simulation).
@@ -63,6 +67,14 @@ def _load():
             lib.pkv_orc_paged_attention.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                                     i32, i32, f64, P, i32]
             lib.pkv_orc_rope.argtypes = [P, i32, f64, f64]
+            lib.pkv_orc_e4m3_to_f64.restype = f64
+            lib.pkv_orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.pkv_orc_f64_to_e4m3.restype = ctypes.c_uint8
+            lib.pkv_orc_f64_to_e4m3.argtypes = [f64]
+            lib.pkv_orc_kv_append_fp8.argtypes = [P, P, P, i32, P, P, i32, i32, i32, P, P]
+            lib.pkv_orc_paged_attention_fp8.restype = i32
+            lib.pkv_orc_paged_attention_fp8.argtypes = [P, P, P, P, P, P, P, i32, P, i32, i32,
+                                                        i32, i32, i32, i32, f64, i32]
             lib.pkv_orc_ring_attention.restype = i32
             lib.pkv_orc_ring_attention.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32,
                                                    i32, i32, i32, i32, i32, f64, i32, f64, P,
@@ -194,3 +206,50 @@ def ring_attention(q, k_cache, v_cache, block_tables, logical_len, high_water, b
                                         block_size, sink, window, float(scale), rope_mode,
                                         float(rope_base), _ptr(mask), num_threads)
     return (out, nt) if return_threads else out
+
+
+# --------------------------------------------------------------------------- FP8 (E4M3) cache
+def e4m3_to_f64(codes) -> np.ndarray:
+    """E4M3 byte codes -> fp64 values (NaN for S.1111.111)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    f = _load().pkv_orc_e4m3_to_f64
+    return np.array([f(int(x)) for x in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def f64_to_e4m3(x) -> np.ndarray:
+    """Round to nearest E4M3 (ties to the even code), saturating finite values to +-448."""
+    a = np.asarray(x, dtype=np.float64)
+    f = _load().pkv_orc_f64_to_e4m3
+    return np.array([f(float(v)) for v in a.ravel()], dtype=np.uint8).reshape(a.shape)
+
+
+def kv_append_fp8(k, v, slots, k_cache, v_cache, block_size, k_scale, v_scale) -> None:
+    """In-place FP8 append: k, v [T, Hkv, D] fp16 -> E4M3(x / scale[h]) bytes in one layer's
+    uint8 pools [NB, Hkv, bs, D]; the division is done in binary32."""
+    k, v, slots = _u16(k), _u16(v), _i64(slots)
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    _load().pkv_orc_kv_append_fp8(_ptr(k), _ptr(v), _ptr(slots), len(slots), _ptr(k_cache),
+                                  _ptr(v_cache), k.shape[1], k.shape[2], block_size, _ptr(ks),
+                                  _ptr(vs))
+
+
+def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                        block_size, scale, num_threads=0):
+    """q [B, q_len, Hq, D] fp16; uint8 E4M3 caches [NB, Hkv, bs, D] with per-kv-head scales
+    -> out fp64 [B, q_len, Hq, D]."""
+    q = _u16(q)
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    bt, cl = _i32(block_tables), _i32(context_lens)
+    B, q_len, Hq, D = q.shape
+    Hkv = kc.shape[1]
+    out = np.zeros(q.shape, dtype=np.float64)
+    _load().pkv_orc_paged_attention_fp8(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks),
+                                        _ptr(vs), _ptr(bt), bt.shape[1], _ptr(cl), B, q_len, Hq,
+                                        Hkv, D, block_size, float(scale), num_threads)
+    return out

@@ -342,4 +342,104 @@ int pkv_orc_ring_attention(double* out, const uint16_t* q, const uint16_t* k_cac
   });
 }
 
+
+// ---------------------------------------------------------------------------
+// FP8 KV cache (E4M3).
+// [VLLM] §工程权衡 (量化与 KV Cache 精度的权衡): quantising the KV cache from FP16
+// to FP8 halves its memory, and production keeps KV at FP8 rather than INT4.
+// The page names no FP8 layout; the reading here is the E4M3 format (1 sign
+// bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 subnormal;
+// S.1111.111 is NaN and there is no infinity, so the largest finite value is
+// 1.75 * 2^8 = 448), one scale per (layer, kv head) for K and one for V:
+// stored code = E4M3(x / scale), value = decode(code) * scale.
+// ---------------------------------------------------------------------------
+double pkv_orc_e4m3_to_f64(uint8_t c) {
+  const int sign = (c >> 7) & 1;
+  const int expo = (c >> 3) & 0xf;
+  const int mant = c & 7;
+  double v;
+  if (expo == 15 && mant == 7) return std::nan("");
+  if (expo == 0)
+    v = std::ldexp(static_cast<double>(mant), -9);             // mant/8 * 2^-6
+  else
+    v = std::ldexp(static_cast<double>(8 + mant), expo - 10);  // (1 + mant/8) * 2^(e-7)
+  return sign ? -v : v;
+}
+
+// Round to the nearest E4M3 value, ties to the even code (mantissa bit 0 clear), finite
+// values beyond the largest saturate to +-448, NaN stays NaN. Plain search over the codes.
+uint8_t pkv_orc_f64_to_e4m3(double x) {
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  if (std::isnan(x)) return sign | 0x7f;
+  const double a = std::fabs(x);
+  if (a >= 448.0) return sign | 0x7e;
+  int best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c <= 0x7e; ++c) {
+    const double err = std::fabs(pkv_orc_e4m3_to_f64(static_cast<uint8_t>(c)) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0)) { best = c; best_err = err; }
+  }
+  return sign | static_cast<uint8_t>(best);
+}
+
+// FP8 append: the FP16 row's elements, divided by their kv head's scale in
+// binary32 (the precision the device takes the quantisation decision in), go
+// to E4M3 codes in the pools' slots. Pools: [NB][Hkv][bs][D] bytes.
+void pkv_orc_kv_append_fp8(const uint16_t* k, const uint16_t* v, const int64_t* slot_mapping,
+                           int num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                           int num_kv_heads, int D, int block_size, const float* k_scale,
+                           const float* v_scale) {
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      const int64_t src = (static_cast<int64_t>(t) * num_kv_heads + h) * D;
+      const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * D;
+      for (int d = 0; d < D; ++d) {
+        const float xk = static_cast<float>(pkv_orc_f16_to_f64(k[src + d])) / k_scale[h];
+        const float xv = static_cast<float>(pkv_orc_f16_to_f64(v[src + d])) / v_scale[h];
+        k_cache[dst + d] = pkv_orc_f64_to_e4m3(xk);
+        v_cache[dst + d] = pkv_orc_f64_to_e4m3(xv);
+      }
+    }
+  }
+}
+
+// Paged decode attention over an FP8 cache: the same gather-then-textbook
+// attention as pkv_orc_paged_attention, each K (V) element being
+// decode(code) * k_scale[kv head] (v_scale) in fp64.
+int pkv_orc_paged_attention_fp8(double* out, const uint16_t* q, const uint8_t* k_cache,
+                                const uint8_t* v_cache, const float* k_scale,
+                                const float* v_scale, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens, int B,
+                                int q_len, int Hq, int Hkv, int D, int block_size, double scale,
+                                int num_threads) {
+  const int G = Hq / Hkv;
+  const int64_t items = static_cast<int64_t>(B) * Hkv;
+  return parallel_for(items, num_threads, [&](int64_t item) {
+    const int b = static_cast<int>(item / Hkv), kvh = static_cast<int>(item % Hkv);
+    const int64_t ctx = context_lens[b];
+    std::vector<double> K(ctx * D), V(ctx * D);
+    for (int64_t t = 0; t < ctx; ++t) {
+      const int64_t phys = block_tables[static_cast<int64_t>(b) * max_blocks_per_seq + t / block_size];
+      const int64_t row = ((phys * Hkv + kvh) * block_size + t % block_size) * D;
+      for (int d = 0; d < D; ++d) {
+        K[t * D + d] = pkv_orc_e4m3_to_f64(k_cache[row + d]) * static_cast<double>(k_scale[kvh]);
+        V[t * D + d] = pkv_orc_e4m3_to_f64(v_cache[row + d]) * static_cast<double>(v_scale[kvh]);
+      }
+    }
+    std::vector<double> qv(D);
+    for (int qi = 0; qi < q_len; ++qi) {
+      const int64_t visible = std::max<int64_t>(0, ctx - q_len + qi + 1);
+      for (int g = 0; g < G; ++g) {
+        const int h = kvh * G + g;
+        const int64_t base = ((static_cast<int64_t>(b) * q_len + qi) * Hq + h) * D;
+        for (int d = 0; d < D; ++d) qv[d] = pkv_orc_f16_to_f64(q[base + d]);
+        attend(qv.data(), K, V, visible, D, scale, out + base);
+      }
+    }
+  });
+}
+
 }  // extern "C"

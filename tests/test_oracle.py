@@ -447,3 +447,104 @@ def test_ring_without_rope_and_wrap_is_paged_attention():
     a = oracle.ring_attention(q, k, v, tables, L, L, 16, 4, 508, 0.09, rope_mode=oracle.ROPE_NONE)
     b = oracle.paged_attention(q, k, v, tables, L.astype(np.int32), 16, 0.09)
     assert np.max(np.abs(a - b)) < 1e-13
+
+
+# ------------------------------------------------------------------------------ FP8 (E4M3) cache
+def _torch_e4m3_decode_all():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_decoder_matches_torch_for_every_code():
+    ours = oracle.e4m3_to_f64(np.arange(256))
+    ref = _torch_e4m3_decode_all()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # the format's landmarks: largest finite, smallest normal and subnormal, NaN codes
+    assert ours[0x7E] == 448.0 and ours[0xFE] == -448.0
+    assert ours[0x08] == 2.0 ** -6 and ours[0x01] == 2.0 ** -9 and ours[0x38] == 1.0
+    assert np.isnan(ours[0x7F]) and np.isnan(ours[0xFF]) and nan.sum() == 2
+
+
+def test_e4m3_encoder_matches_torch_rounding_in_range():
+    rng = np.random.default_rng(11)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 4.0,
+        rng.standard_normal(5000) * 2.0 ** -7,          # subnormal range
+        rng.uniform(-447.0, 447.0, 5000),
+        # exact ties between neighbouring codes: midpoints of every finite pair
+        (lambda v: 0.5 * (v[:-1] + v[1:]))(np.sort(_torch_e4m3_decode_all()[:0x7F])),
+    ]).astype(np.float32)
+    ours = oracle.f64_to_e4m3(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_encoder_nearest_ties_even_and_saturates():
+    values = oracle.e4m3_to_f64(np.arange(0x7F))            # 0 .. 448, increasing
+    assert np.all(np.diff(values) > 0)
+    rng = np.random.default_rng(12)
+    for x in rng.uniform(0.0, 448.0, 300):
+        c = int(oracle.f64_to_e4m3(x))
+        assert abs(values[c] - x) == np.min(np.abs(values - x))
+    # ties go to the even code: 1.0625 lies halfway between 1.0 (0x38) and 1.125 (0x39)
+    assert oracle.f64_to_e4m3(1.0625) == 0x38 and oracle.f64_to_e4m3(1.1875) == 0x3A
+    # finite values past the largest normal saturate; the sign is kept, zero too
+    assert oracle.f64_to_e4m3(1000.0) == 0x7E and oracle.f64_to_e4m3(-1e6) == 0xFE
+    assert oracle.f64_to_e4m3(-1e-9) == 0x80 and oracle.f64_to_e4m3(0.0) == 0x00
+    # decode(encode(v)) == v for every finite code
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert oracle.f64_to_e4m3(oracle.e4m3_to_f64(c)) == c
+
+
+def test_kv_append_fp8_quantises_in_binary32_and_touches_only_its_slots():
+    rng = np.random.default_rng(13)
+    nb, hkv, bs, d, T = 6, 2, 16, 128, 5
+    k = rng.standard_normal((T, hkv, d)).astype(np.float16)
+    v = rng.standard_normal((T, hkv, d)).astype(np.float16)
+    ks = np.array([0.05, 0.37], np.float32)
+    vs = np.array([0.11, 0.023], np.float32)
+    slots = np.array([3, 17, -1, 95, 40], np.int64)
+    kc = rng.integers(0, 256, (nb, hkv, bs, d), dtype=np.uint8)
+    vc = rng.integers(0, 256, (nb, hkv, bs, d), dtype=np.uint8)
+    kc0, vc0 = kc.copy(), vc.copy()
+    oracle.kv_append_fp8(k, v, slots, kc, vc, bs, ks, vs)
+    ek, ev = kc0.copy(), vc0.copy()
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        for h in range(hkv):
+            xk = torch.from_numpy(k[t, h].astype(np.float32) / ks[h])
+            xv = torch.from_numpy(v[t, h].astype(np.float32) / vs[h])
+            ek[s // bs, h, s % bs] = xk.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            ev[s // bs, h, s % bs] = xv.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
+
+
+def test_fp8_attention_equals_fp16_attention_on_the_dequantised_cache():
+    # with power-of-two scales every dequantised value is exact in fp16, so the FP8 oracle
+    # must give exactly the fp16 oracle's result on that fp16 cache
+    rng = np.random.default_rng(14)
+    nb, hkv, hq, bs, d = 24, 2, 12, 16, 128
+    lens = np.array([37, 100, 1, 64], np.int32)
+    perm = rng.permutation(nb).astype(np.int32)
+    bt = np.full((len(lens), 8), -1, np.int32)
+    o = 0
+    for b, L in enumerate(lens):
+        n = -(-int(L) // bs)
+        bt[b, :n] = perm[o:o + n]
+        o += n
+    kc8 = rng.integers(0, 256, (nb, hkv, bs, d), dtype=np.uint8)
+    vc8 = rng.integers(0, 256, (nb, hkv, bs, d), dtype=np.uint8)
+    kc8[(kc8 & 0x7F) == 0x7F] = 0x11                    # no NaN codes in the cache
+    vc8[(vc8 & 0x7F) == 0x7F] = 0x22
+    ks = np.array([2.0 ** -3, 2.0 ** -6], np.float32)
+    vs = np.array([2.0 ** -4, 1.0], np.float32)
+    q = rng.standard_normal((len(lens), 1, hq, d)).astype(np.float16)
+    got = oracle.paged_attention_fp8(q, kc8, vc8, ks, vs, bt, lens, bs, 1 / math.sqrt(d))
+    kf = (oracle.e4m3_to_f64(kc8) * ks[None, :, None, None]).astype(np.float16)
+    vf = (oracle.e4m3_to_f64(vc8) * vs[None, :, None, None]).astype(np.float16)
+    assert np.array_equal(kf.astype(np.float64), oracle.e4m3_to_f64(kc8) * ks[None, :, None, None])
+    want = oracle.paged_attention(q, kf, vf, bt, lens, bs, 1 / math.sqrt(d))
+    assert np.array_equal(got, want)
