@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the CPU-baseline sample")
+    ap.add_argument("--kv", choices=["fp16", "fp8"], default="fp16",
+                    help="fp8: an E4M3 cache with per-kv-head scales (paged GQA workloads): per "
+                         "layer the FP8 append of the step's rows, then FP8 decode attention")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers than the workload's (small profiler captures; the "
                          "per-launch figures are unchanged, the step and the L2 note shrink)")
@@ -72,9 +75,12 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-def step_bytes(w) -> int:
-    """Algorithmic fp16 K+V bytes one step reads over all layers: every visible token of every
-    (sequence, kv head) once (for the ring, the min(hw, sink + window) slots it holds)."""
+def step_bytes(w, kv="fp16") -> int:
+    """Algorithmic K+V bytes one step reads over all layers: every visible token of every
+    (sequence, kv head) once (for the ring, the min(hw, sink + window) slots it holds); an E4M3
+    cache holds one byte per element instead of two."""
+    if kv == "fp8":
+        return w.kv_read_bytes() // 2
     if w.name == "ring":
         hw = w.context_lens.astype(np.int64)          # L = hw: no rollback in this step
         toks = int(np.minimum(hw, w.sink + w.window).sum())
@@ -93,9 +99,9 @@ def unique_bytes(w) -> int:
     return sum(used.values()) * w.num_kv_heads * w.head_dim * 2 * 2 * w.num_layers
 
 
-def describe(w) -> dict:
+def describe(w, kv="fp16") -> dict:
     cl = w.context_lens.astype(np.int64)
-    nbytes = step_bytes(w)
+    nbytes = step_bytes(w, kv)
     return {
         "workload": w.name,
         "layers": w.num_layers, "num_seqs": w.num_seqs, "q_len": w.q_len,
@@ -165,16 +171,33 @@ class ClockSampler:
 class Step:
     """Device-resident inputs of one decode step and the launches that make it."""
 
-    def __init__(self, w, dev, seed_offset=0):
+    def __init__(self, w, dev, seed_offset=0, kv="fp16"):
         from paged_kv_cache_147_gb300 import pkv
         self.pkv = pkv
         self.w = w
         self.dev = dev
-        # fused append + decode per layer (paged workloads), decode only (prefix), or the
-        # sink + ring decode (ring)
+        # fused append + decode per layer (paged workloads), decode only (prefix), the sink +
+        # ring decode (ring), or FP8 append + FP8 decode per layer (an E4M3 cache)
         self.kind = {"prefix": "decode", "ring": "ring"}.get(w.name, "fused")
+        if kv == "fp8":
+            if self.kind != "fused":
+                raise SystemExit("--kv fp8 applies to the paged GQA workloads")
+            self.kind = "fp8"
         Lr = w.num_layers
         self.k, self.v = w.pools(dev)
+        if self.kind == "fp8":
+            # E4M3 pools from the same data, one scale per (layer, kv head): max |x| / 448
+            k8 = torch.empty(self.k.shape, dtype=torch.uint8, device=dev)
+            v8 = torch.empty(self.v.shape, dtype=torch.uint8, device=dev)
+            self.ks = torch.empty((Lr, w.num_kv_heads), dtype=torch.float32, device=dev)
+            self.vs = torch.empty_like(self.ks)
+            for l in range(Lr):
+                for src, dst, sc in ((self.k, k8, self.ks), (self.v, v8, self.vs)):
+                    x = src[l].float()
+                    sc[l] = x.abs().amax(dim=(0, 2, 3)) / 448.0
+                    y = (x / sc[l][None, :, None, None]).clamp(-448.0, 448.0)
+                    dst[l] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+            self.k, self.v = k8, v8
         self.bt = torch.as_tensor(w.block_tables, device=dev)
         self.cl = torch.as_tensor(w.context_lens, device=dev)
         seq, pos = w.new_token_positions()
@@ -187,7 +210,7 @@ class Step:
         self.out = torch.empty_like(self.q)
         self.slots = torch.empty(seq.shape[0], dtype=torch.int64, device=dev)
         self.ws = pkv.make_workspace(w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, dev)
-        self.launches_per_step = Lr
+        self.launches_per_step = 2 * Lr + 1 if self.kind == "fp8" else Lr
         if self.kind == "ring":
             self.L = torch.as_tensor(w.context_lens.astype(np.int64), device=dev)
             self.hw = self.L.clone()
@@ -199,6 +222,15 @@ class Step:
         p, w = self.pkv, self.w
         if self.kind == "decode":
             return self.run_decode_only()
+        if self.kind == "fp8":
+            p.slot_mapping(self.seq, self.pos, self.bt, w.block_size, out=self.slots)
+            for l in range(w.num_layers):
+                p.kv_append_fp8(self.kn[l], self.vn[l], self.slots, self.k[l], self.v[l],
+                                self.ks[l], self.vs[l])
+                p.paged_attn_decode_fp8(self.out[l], self.q[l], self.k[l], self.v[l],
+                                        self.ks[l], self.vs[l], self.bt, self.cl, w.scale,
+                                        self.ws)
+            return
         for l in range(w.num_layers):
             if self.kind == "ring":
                 p.ring_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.L,
@@ -220,6 +252,12 @@ class Step:
         p, w = self.pkv, self.w
         if self.kind == "ring":
             return self.run()
+        if self.kind == "fp8":
+            for l in range(w.num_layers):
+                p.paged_attn_decode_fp8(self.out[l], self.q[l], self.k[l], self.v[l],
+                                        self.ks[l], self.vs[l], self.bt, self.cl, w.scale,
+                                        self.ws)
+            return
         for l in range(w.num_layers):
             p.paged_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.cl,
                                 w.scale, self.ws)
@@ -237,11 +275,15 @@ class Step:
             return f"CUDA graph: {n} x paged_attn_decode (decode only)"
         if self.kind == "ring":
             return f"CUDA graph: {n} x ring_attn_decode ({self.w.q_len} causal draft queries)"
+        if self.kind == "fp8":
+            return (f"CUDA graph: slot_mapping, then {n} x (kv_append_fp8 + "
+                    "paged_attn_decode_fp8)")
         return (f"CUDA graph: {n} x paged_attn_decode_append "
                 "(slot mapping + KV append + decode, one launch)")
 
     def kernel_note(self) -> str:
         return {"decode": "decode_kernel (paged_attn_decode)",
+                "fp8": "decode_kernel, E4M3 cache (paged_attn_decode_fp8)",
                 "ring": "decode_kernel, sink + ring with RoPE on read (ring_attn_decode)"}.get(
             self.kind, "decode_kernel, fused append (paged_attn_decode_append)")
 
@@ -389,7 +431,7 @@ def run_ours(args, w, rank, local_rank, world_size):
     torch.cuda.set_device(local_rank)
     from paged_kv_cache_147_gb300 import pkv
     pkv.load()
-    st = Step(w, dev)
+    st = Step(w, dev, kv=args.kv)
     step_graph = capture(st.run)
     decode_graph = capture(st.run_decode_only)
 
@@ -397,7 +439,7 @@ def run_ours(args, w, rank, local_rank, world_size):
     clocks.start()
     elapsed = time_replays(step_graph, args.steps, args.warmup)
     clk = clocks.stop()
-    bytes_step = step_bytes(w)
+    bytes_step = step_bytes(w, args.kv)
     t_max, total_bytes = replicas.aggregate(elapsed, float(bytes_step) * args.steps,
                                             device=dev)
     value = total_bytes / t_max / 1e9
@@ -405,12 +447,14 @@ def run_ours(args, w, rank, local_rank, world_size):
     # dominant kernel: the decode launch is the whole step; its average launch duration is
     # the step time over its launches (they run back to back, the fused ones each overlapping
     # the previous one's tail). The unfused decode is timed alone as well. For the prefix batch
-    # the roofline counts the distinct block rows (the shared prefix once).
+    # the roofline counts the distinct block rows (the shared prefix once). With the E4M3
+    # cache a layer is an FP8 append plus the decode: launch_us is their sum, and the decode
+    # alone is unfused_decode_launch_us.
     per_launch = (t_max / args.steps) / w.num_layers
     bytes_launch = (unique_bytes(w) if w.name == "prefix" else bytes_step) / w.num_layers
     peak, peak_kind = load_peaks()
     achieved = bytes_launch / per_launch / 1e9
-    traffic = traffic_record(w)
+    traffic = traffic_record(w) if args.kv == "fp16" else None
     dsteps = max(10, args.steps // 2)
     plain_per_launch = time_replays(decode_graph, dsteps, args.warmup) / (dsteps * w.num_layers)
     append_per_launch = None
@@ -429,8 +473,9 @@ def run_ours(args, w, rank, local_rank, world_size):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world_size,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t_max / args.steps * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": describe(w) | {"graph": st.graph_note(),
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 K/V, f16 q/out" if args.kv == "fp8" else "f16", "data": "synthetic",
+        "config": describe(w, args.kv) | {"graph": st.graph_note(), "kv": args.kv,
                                  "parallelism": f"replicas x{world_size}"},
         "decode_tokens_per_s": round(w.num_seqs * w.q_len * args.steps * world_size / t_max, 1),
         "pct_of_nominal_8tbs": round(100 * value / world_size / NOMINAL_HBM_GBS, 2),
@@ -552,7 +597,7 @@ def main():
     replicas.init()
     line = run_ours(args, w, rank, local_rank, world_size)
     if rank == 0:
-        if not args.no_cpu_baseline and w.name != "ring":
+        if not args.no_cpu_baseline and w.name != "ring" and args.kv == "fp16":
             line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     replicas.shutdown()

@@ -215,6 +215,35 @@ int pkv_ring_attn_decode(void* out, const void* q, const void* k_cache, const vo
                          float scale, void* workspace, size_t workspace_bytes,
                          pkv_stream_t stream);
 
+/* ---- FP8 (E4M3) KV cache -------------------------------------------------------------------
+ * [VLLM] §工程权衡 (量化与 KV Cache 精度的权衡): FP8 halves the KV cache and is the conservative
+ * choice for KV (rather than INT4). The page fixes no layout; here the pools hold E4M3 bytes
+ * (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; S.1111.111 is NaN; largest finite
+ * 448) in the fp16 pools' layout [num_blocks][num_kv_heads][block_size][head_dim], one byte per
+ * element, and every (layer, kv head) has a K and a V scale: element value = code * scale.
+ * k_scale, v_scale (device): float [num_kv_heads], positive, owned by the caller.
+ *
+ * pkv_kv_append_fp8: pkv_kv_append's scatter, each element stored as E4M3(x / scale[kh]): the
+ * fp16 value is divided by the scale in binary32 and rounded to nearest (ties to even), finite
+ * values past 448 saturate to +-448. Same slot rules and errors as pkv_kv_append; k, v fp16
+ * [num_tokens][num_kv_heads][head_dim] (16-byte aligned), caches 16-byte aligned. */
+int pkv_kv_append_fp8(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                      void* k_cache, void* v_cache, int num_blocks, int num_kv_heads,
+                      int head_dim, int block_size, const float* k_scale, const float* v_scale,
+                      pkv_stream_t stream);
+
+/* pkv_paged_attn_decode over an E4M3 cache: K_t = code * k_scale[kh], V_t = code * v_scale[kh]
+ * (the codes are widened to fp16 exactly, the scales applied in fp32 to the scores and the
+ * output). Requires (num_q_heads / num_kv_heads) * q_len <= 8; otherwise PKV_EINVAL. Other
+ * arguments, workspace and errors as for pkv_paged_attn_decode. */
+int pkv_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache,
+                              const void* v_cache, const float* k_scale, const float* v_scale,
+                              int num_blocks, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                              int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, float scale, void* workspace,
+                              size_t workspace_bytes, pkv_stream_t stream);
+
 /* ---- host-side validation (debug mode; all arrays are HOST copies) ---------------------------
  * pkv_check_tables: every block-table entry a sequence uses (the first
  * ceil(context_lens[b]/block_size)) is in [0, num_blocks), and 0 <= context_lens[b] <=

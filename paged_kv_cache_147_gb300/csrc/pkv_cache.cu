@@ -92,6 +92,53 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __res
     v_cache[dst] = __ldg(v + src);
 }
 
+// fp32 pair -> E4M3 pair (first value in the low byte): round to nearest even, finite
+// values past 448 saturate.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+
+// FP8 append: thread = 8 consecutive elements of one (token, K|V, kv head) row: 16 fp16 bytes
+// in, each divided by the head's scale in binary32 and rounded to E4M3, 8 bytes out.
+__global__ void kv_append_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                     const int64_t* __restrict__ slots, int num_tokens,
+                                     uint2* __restrict__ k_cache, uint2* __restrict__ v_cache,
+                                     int64_t num_slots, int num_kv_heads, int vecs_per_row,
+                                     int block_size, const float* __restrict__ k_scale,
+                                     const float* __restrict__ v_scale, unsigned int* err) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t per_token = static_cast<int64_t>(2) * num_kv_heads * vecs_per_row;
+  if (idx >= per_token * num_tokens) return;
+  const int t = static_cast<int>(idx / per_token);
+  int64_t rem = idx - t * per_token;
+  const int which = static_cast<int>(rem / (static_cast<int64_t>(num_kv_heads) * vecs_per_row));
+  rem -= static_cast<int64_t>(which) * num_kv_heads * vecs_per_row;
+  const int h = static_cast<int>(rem / vecs_per_row);
+  const int c = static_cast<int>(rem % vecs_per_row);
+  const int64_t slot = slots[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (c == 0 && which == 0 && h == 0) atomicOr(err, PKV_DEVERR_SLOT);
+    return;
+  }
+  const int64_t blk = slot / block_size, off = slot % block_size;
+  const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * vecs_per_row + c;
+  const int64_t src = (static_cast<int64_t>(t) * num_kv_heads + h) * vecs_per_row + c;
+  const uint4 x = __ldg((which ? v : k) + src);
+  const float sc = __ldg((which ? v_scale : k_scale) + h);
+  const __half2* hx = reinterpret_cast<const __half2*>(&x);
+  uint32_t q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(hx[i]);
+    q[i] = f32x2_to_e4m3x2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc));
+  }
+  (which ? v_cache : k_cache)[dst] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
 // grid.y enumerates (layer, pair, K|V); grid.x strides over the block's 16-byte vectors.
 __global__ void copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                                    const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
@@ -177,6 +224,33 @@ int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, num_tokens,
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
       static_cast<int64_t>(num_blocks) * block_size, num_kv_heads, vecs, block_size, err);
+  return launch_status();
+}
+
+int pkv_kv_append_fp8(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                      void* k_cache, void* v_cache, int num_blocks, int num_kv_heads,
+                      int head_dim, int block_size, const float* k_scale, const float* v_scale,
+                      pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      head_dim % 8 != 0 || !valid_block_size(block_size))
+    return PKV_EINVAL;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    return PKV_EINVAL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_EINVAL;
+  unsigned int* err = device_error_ptr();
+  if (!err) return launch_status();
+  const int vecs = head_dim / 8;
+  const int64_t total = static_cast<int64_t>(num_tokens) * 2 * num_kv_heads * vecs;
+  const int64_t blocks = (total + kThreads - 1) / kThreads;
+  if (blocks > 0x7fffffff) return PKV_EINVAL;
+  kv_append_fp8_kernel<<<static_cast<unsigned>(blocks), kThreads, 0,
+                         static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, num_tokens,
+      static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache),
+      static_cast<int64_t>(num_blocks) * block_size, num_kv_heads, vecs, block_size, k_scale,
+      v_scale, err);
   return launch_status();
 }
 

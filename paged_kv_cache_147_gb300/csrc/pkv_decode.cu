@@ -108,6 +108,9 @@ struct DecodeArgs {
   const __half* v_new;
   __half* k_pool;
   __half* v_pool;
+  // FP8 (E4M3) cache: per kv head scales of K and V (value = code * scale)
+  const float* k_scale;
+  const float* v_scale;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -118,12 +121,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // ---------------------------------------------------------------------------------------------
 // Shared-memory layout (offsets from a 1024-byte aligned base).
-template <int NCW, int NST, int MT>
+template <int NCW, int NST, int MT, bool FP8 = false>
 struct Smem {
   static constexpr int kNST = NST;
+  // a stage holds one chunk's K and V: fp16 (8 KB) or E4M3 (4 KB: two 16 x 128-byte tiles,
+  // each consumer warp expanding its chunks into an 8 KB fp16 scratch tile of its own)
+  static constexpr int kStage = FP8 ? 2 * kChunk * kD : kStageBytes;
+  static constexpr int kScratch = NST * kStage;        // FP8: NCW x 8 KB fp16 tiles
   static constexpr int kQHalf = MT * 2048;            // 16*MT rows x 128 B
   static constexpr int kQBuf = 2 * kQHalf;
-  static constexpr int kQ = NST * kStageBytes;
+  static constexpr int kQ = kScratch + (FP8 ? NCW * kStageBytes : 0);
   // full[NST], empty[NST], qfull[2], qempty[2], sdone[2], sfree[2]
   static constexpr int kBars = kQ + 2 * kQBuf;
   static constexpr int kFlags = kBars + (2 * NST + 8) * 8;  // abort, pending count + units
@@ -464,6 +471,41 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
   merge_sync<NT>();                        // stage memory free for the next merge
 }
 
+// E4M3 pair (low byte first) -> fp16 pair, exact (every E4M3 value is an fp16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Expands one chunk's E4M3 K and V tiles (16 rows x 128 bytes each, 128B-swizzled as the tensor
+// copy lays them out) into fp16 tiles laid out as an fp16 stage is (per tile two 64-column
+// halves of 16 rows x 128 bytes, 128B-swizzled), so that the fp16 fragment loads read them
+// unchanged. One warp: lane-owned 16-byte pieces, 16 codes in, 32 bytes out.
+__device__ __forceinline__ void expand_e4m3_chunk(uint32_t src, uint32_t dst, int lane) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int item = it * 32 + lane;                 // (tile, row, 16-byte piece)
+    const int tile = item >> 7, r = (item >> 3) & 15, c8 = item & 7;
+    const uint4 v = ld_shared_v4(src + tile * 2048 + swz128(r, c8));
+    uint4 lo, hi;
+    lo.x = e4m3x2_to_f16x2(v.x & 0xffffu);
+    lo.y = e4m3x2_to_f16x2(v.x >> 16);
+    lo.z = e4m3x2_to_f16x2(v.y & 0xffffu);
+    lo.w = e4m3x2_to_f16x2(v.y >> 16);
+    hi.x = e4m3x2_to_f16x2(v.z & 0xffffu);
+    hi.y = e4m3x2_to_f16x2(v.z >> 16);
+    hi.z = e4m3x2_to_f16x2(v.w & 0xffffu);
+    hi.w = e4m3x2_to_f16x2(v.w >> 16);
+    // codes 16 c8 .. 16 c8 + 15 are fp16 columns in half c8 / 4, pieces 2 c8 % 8 and + 1
+    const uint32_t base = dst + tile * 2 * kHalfBytes + (c8 >> 2) * kHalfBytes;
+    const int cc = (2 * c8) & 7;
+    st_shared_v4(base + swz128(r, cc), lo);
+    st_shared_v4(base + swz128(r, cc + 1), hi);
+  }
+}
+
 // Requests segment kk's queries (and, fused append, its new K/V rows) into query buffer kk & 1,
 // completing on that buffer's full barrier; waits first until the consumers have released the
 // buffer's previous use. One thread.
@@ -494,11 +536,11 @@ __device__ __forceinline__ void issue_queries(const DecodeArgs& a, const CUtenso
 // Warp roles: warps 0..NCW-1 consume chunks, warp NCW produces (TMA), warp NCW+1 is the
 // epilogue (merges each segment's per-warp states, writes outputs and split-unit partials,
 // announces arrivals), so the consumers never stop at a unit boundary.
-template <int NCW, int NST, int MT, bool RING, bool APPEND, bool TR>
+template <int NCW, int NST, int MT, bool RING, bool APPEND, bool TR, bool FP8>
 __global__ void __launch_bounds__((NCW + 2) * 32, MT == 1 ? kMinCtasMt1 : 1)
 decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
-  using L = Smem<NCW, NST, MT>;
+  using L = Smem<NCW, NST, MT, FP8>;
   // Stage st holds the CTA's chunks st, st + NST, ... and chunk j goes to consumer warp
   // j % NCW. With NST a multiple of NCW every use of a stage goes to the same warp, which
   // takes them in order, so it never waits on a full-barrier phase more than one ahead of the
@@ -506,6 +548,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   static_assert(NST % NCW == 0, "pipeline stages must be a multiple of the consumer warps");
   static_assert(!(RING && APPEND), "the ring variant appends through its own slot mapping");
   static_assert(!TR || (MT == 1 && !RING), "the transposed tile is for up to 8 rows, paged");
+  static_assert(!FP8 || (TR && !APPEND), "the E4M3 cache is read by the transposed tile only");
   // the queries' buffer stays in use for the whole segment when its fragments are not kept in
   // registers, or when it also holds the segment's new K/V rows
   constexpr bool kHoldQ = MT != 1 || APPEND;
@@ -678,7 +721,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (j >= NST && !mbar_wait(bar_empty + st * 8, ((j / NST) - 1) & 1, abort))
               flag_timeout(a, abort);
             if (APPEND) srow_s[st] = r;   // published to the consumer by the barrier below
-            mbar_arrive_expect_tx(fb, kStageBytes);
+            mbar_arrive_expect_tx(fb, L::kStage);
           }
           __syncwarp();                   // the stage is free before any lane writes it
           // The chunk's four 2 KB boxes (K and V, two 64-column halves each) go out as one
@@ -686,9 +729,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           // cycles, and one thread issuing all four held each chunk up ~150 ns. K/V are read
           // once per step: first to go from L2, which then keeps the partials, queries and
           // tables the merges and other CTAs need.
-          if (lane < 4)
+          if (FP8) {
+            // E4M3: one 2 KB box (16 rows x 128 bytes) each for K and V
+            if (lane < 2)
+              tma_load_2d_hint(sbase + st * L::kStage + lane * (kChunk * kD), lane ? &tmV : &tmK,
+                               0, r, fb, kv_policy);
+          } else if (lane < 4) {
             tma_load_2d_hint(sbase + st * kStageBytes + lane * kHalfBytes, lane < 2 ? &tmK : &tmV,
                              (lane & 1) * 64, r, fb, kv_policy);
+          }
         }
       }
       ++k;
@@ -839,12 +888,24 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const int qi = r < a.R ? r / a.G : a.q_len - 1;
         tlim[e] = Lc - a.q_len + qi + 1;
       }
+      // E4M3 cache: the kv head's K scale joins the score scale, its V scale the output
+      const float score_l2 = FP8 ? a.scale_log2 * __ldg(a.k_scale + s.h) : a.scale_log2;
+      const float out_sc = FP8 ? __ldg(a.v_scale + s.h) : 1.f;
       const int nchunk = s.c1 - s.c0;
       for (int jj = ((w - j) % NCW + NCW) % NCW; jj < nchunk; jj += NCW) {
         const int gj = j + jj;
         const int st = gj % NST;
         if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
-        const uint32_t stK = sbase + st * kStageBytes;
+        uint32_t stK = sbase + st * L::kStage;
+        if constexpr (FP8) {
+          // expand into this warp's fp16 tiles (its previous chunk's reads are done), then
+          // free the stage at once
+          stK = sbase + L::kScratch + w * kStageBytes;
+          __syncwarp();
+          expand_e4m3_chunk(sbase + st * L::kStage, stK, lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_empty + st * 8);
+        }
         const uint32_t stV = stK + 2 * kHalfBytes;
         const int c = s.c0 + jj;
         const bool full_chunk = (c + 1) * kChunk <= Lc - a.q_len + 1;
@@ -890,8 +951,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int pos0 = c * kChunk + g, pos1 = pos0 + 8;
-          float x0 = (sa[e] + sb2[e]) * a.scale_log2;
-          float x1 = (sa[2 + e] + sb2[2 + e]) * a.scale_log2;
+          float x0 = (sa[e] + sb2[e]) * score_l2;
+          float x1 = (sa[2 + e] + sb2[2 + e]) * score_l2;
           if (!full_chunk) {
             x0 = pos0 < tlim[e] ? x0 : kNegInf;
             x1 = pos1 < tlim[e] ? x1 : kNegInf;
@@ -941,8 +1002,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           mma_16816(ot[dt], v0, v2, v1, v3, pb0, pb1);
         }
         if (APPEND && patched) fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + st * 8);
+        if (!FP8) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_empty + st * 8);
+        }
       }
       if (kHoldQ) {
         __syncwarp();
@@ -964,8 +1027,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           float* dst = o_d + (w * a.R + r) * kSt + g;
 #pragma unroll
           for (int dt = 0; dt < 8; ++dt) {
-            dst[16 * dt] = ot[dt][e];
-            dst[16 * dt + 8] = ot[dt][2 + e];
+            dst[16 * dt] = FP8 ? ot[dt][e] * out_sc : ot[dt][e];
+            dst[16 * dt + 8] = FP8 ? ot[dt][2 + e] * out_sc : ot[dt][2 + e];
           }
           if (g == 0) {
             stM[(sb * NCW + w) * a.R + r] = tm[e];
@@ -1265,7 +1328,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const int t = warp < NCW ? tid : tid - 32;   // dense index over consumers + epilogue
     const int ua = unit_first(pre, a.Hkv, last_b, last_h, last_nb);
     const int parts = (ua + last_nb - 1) / per - ua / per + 1;
-    const MergeStage ms(smem, NST * kStageBytes, a.R);
+    const MergeStage ms(smem, L::kQ, a.R);
     named_barrier_sync(2, kNE);                  // last states written, earlier segments merged
     const int sb = last_k & 1;
     float* so_w = stO + sb * NCW * a.R * kSt;
@@ -1295,7 +1358,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       named_barrier_sync(2, kNE);
       merged = *fast_s;
       if (merged) {
-        merge_unit<kNE>(a, last_b, last_h, last_nb, pre, per, smem, NST * kStageBytes, t,
+        merge_unit<kNE>(a, last_b, last_h, last_nb, pre, per, smem, L::kQ, t,
                         blockIdx.x);
       } else {
         // give up waiting: the staged partial goes to the workspace like the others'
@@ -1326,7 +1389,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 #pragma unroll 1
     for (int i = 0; i < np; ++i)
       merge_unit<kNE>(a, npend_s[1 + 3 * i], npend_s[2 + 3 * i], npend_s[3 + 3 * i], pre, per,
-                      smem, NST * kStageBytes, t);
+                      smem, L::kQ, t);
   }
 }
 
@@ -1338,6 +1401,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 // read) and are bound by the consumers' arithmetic: four consumer warps, eight stages.
 constexpr int kNCW = PKV_DECODE_WARPS, kNST = PKV_DECODE_STAGES;
 constexpr int kNCWRing = 4, kNSTRing = 8;
+// The E4M3 cache: 4 KB stages plus an 8 KB fp16 tile per consumer warp, within the shared
+// memory of the fp16 kernels (two CTAs per SM). Widening the codes costs each consumer warp
+// about as much as its mma work, so four consumer warps share the chunks (eight stages, 32 KB
+// of K/V in flight per CTA: half the bytes of the fp16 kernels' chunks).
+#ifndef PKV_FP8_WARPS
+#define PKV_FP8_WARPS 4
+#endif
+#ifndef PKV_FP8_STAGES
+#define PKV_FP8_STAGES 8
+#endif
+constexpr int kNCWFp8 = PKV_FP8_WARPS, kNSTFp8 = PKV_FP8_STAGES;
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, DecodeArgs);
 
@@ -1349,16 +1423,18 @@ struct Variant {
   size_t (*smem)(int R, int B, int newkv_bytes);
 };
 
-template <int NCW, int NST, int MT>
+template <int NCW, int NST, int MT, bool FP8 = false>
 size_t smem_of(int R, int B, int newkv_bytes) {
-  return Smem<NCW, NST, MT>::bytes(R, B, newkv_bytes);
+  return Smem<NCW, NST, MT, FP8>::bytes(R, B, newkv_bytes);
 }
 
-template <int MT, bool RING, bool APPEND, bool TR = false>
+template <int MT, bool RING, bool APPEND, bool TR = false, bool FP8 = false>
 Variant variant() {
-  constexpr int NCW = RING ? kNCWRing : kNCW, NST = RING ? kNSTRing : kNST;
-  return Variant{reinterpret_cast<const void*>(&decode_kernel<NCW, NST, MT, RING, APPEND, TR>),
-                 MT, RING, (NCW + 2) * 32, &smem_of<NCW, NST, MT>};
+  constexpr int NCW = RING ? kNCWRing : FP8 ? kNCWFp8 : kNCW;
+  constexpr int NST = RING ? kNSTRing : FP8 ? kNSTFp8 : kNST;
+  return Variant{
+      reinterpret_cast<const void*>(&decode_kernel<NCW, NST, MT, RING, APPEND, TR, FP8>), MT,
+      RING, (NCW + 2) * 32, &smem_of<NCW, NST, MT, FP8>};
 }
 
 // Persistent grid for a variant: SM count x resident CTAs (capped), cached per device/size.
@@ -1406,11 +1482,12 @@ WsLayout ws_layout(int num_seqs, int Hkv, int R) {
 }
 
 int encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-           const cuuint64_t* strides, const cuuint32_t* box) {
+           const cuuint64_t* strides, const cuuint32_t* box,
+           CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_FLOAT16) {
   auto fn = tensor_map_encoder();
   if (!fn) return PKV_ECUDA_BASE - static_cast<int>(cudaErrorNotSupported);
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(base), dims,
+  CUresult r = fn(map, type, rank, const_cast<void*>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PKV_OK : PKV_EINVAL;
@@ -1422,7 +1499,8 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
                   const int32_t* context_lens, const int64_t* logical_len,
                   const int64_t* high_water, int num_seqs, int q_len, int Hq, int Hkv,
                   int head_dim, int block_size, int sink, int window, const float* rope,
-                  float scale, void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+                  float scale, void* workspace, size_t workspace_bytes, pkv_stream_t stream,
+                  const float* k_scale = nullptr, const float* v_scale = nullptr) {
   if (num_seqs < 0 || q_len < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || head_dim != kD ||
       !valid_block_size(block_size) || num_blocks < 0 || max_blocks < 0)
     return PKV_EINVAL;
@@ -1437,6 +1515,8 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
     return PKV_EINVAL;
   const bool append = k_new != nullptr;
   if (append && (ring || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
+  const bool fp8 = k_scale != nullptr;
+  if (fp8 && (ring || append || !v_scale || G * q_len > 8)) return PKV_EINVAL;
   if (ring) {
     if (!logical_len || !high_water || !rope || sink < 0 || window < 1) return PKV_EINVAL;
     if ((sink + window + block_size - 1) / block_size > max_blocks) return PKV_EINVAL;
@@ -1455,7 +1535,8 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   const int mt = R <= 16 ? 1 : 2;
   // up to 8 rows per unit (GQA groups of 6-8 at one query token): the transposed tile
   const bool tr = !ring && R <= 8;
-  Variant v = ring     ? (mt == 1 ? variant<1, true, false>() : variant<2, true, false>())
+  Variant v = fp8      ? variant<1, false, false, true, true>()
+              : ring   ? (mt == 1 ? variant<1, true, false>() : variant<2, true, false>())
               : append ? (tr ? variant<1, false, true, true>()
                              : mt == 1 ? variant<1, false, true>() : variant<2, false, true>())
                        : (tr ? variant<1, false, false, true>()
@@ -1467,11 +1548,14 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   if (!grid) return status != PKV_OK ? status : PKV_EINVAL;
 
   CUtensorMap tmK, tmV, tmQ;
+  // rows of 128 fp16 (two 64-column boxes per chunk) or of 128 E4M3 bytes (one box)
   const cuuint64_t kv_dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t kv_strides[1] = {kD * 2};
-  const cuuint32_t kv_box[2] = {64, kChunk};
-  int st = encode(&tmK, k_cache, 2, kv_dims, kv_strides, kv_box);
-  if (st == PKV_OK) st = encode(&tmV, v_cache, 2, kv_dims, kv_strides, kv_box);
+  const cuuint64_t kv_strides[1] = {static_cast<cuuint64_t>(fp8 ? kD : kD * 2)};
+  const cuuint32_t kv_box[2] = {static_cast<cuuint32_t>(fp8 ? kD : 64), kChunk};
+  const CUtensorMapDataType kv_type =
+      fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  int st = encode(&tmK, k_cache, 2, kv_dims, kv_strides, kv_box, kv_type);
+  if (st == PKV_OK) st = encode(&tmV, v_cache, 2, kv_dims, kv_strides, kv_box, kv_type);
   const cuuint64_t q_dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(Hq),
                                 static_cast<cuuint64_t>(num_seqs) * q_len};
   const cuuint64_t q_strides[2] = {kD * 2, static_cast<cuuint64_t>(Hq) * kD * 2};
@@ -1512,6 +1596,8 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   args.v_new = static_cast<const __half*>(v_new);
   args.k_pool = static_cast<__half*>(const_cast<void*>(k_cache));
   args.v_pool = static_cast<__half*>(const_cast<void*>(v_cache));
+  args.k_scale = k_scale;
+  args.v_scale = v_scale;
 
   void* params[4] = {&tmK, &tmV, &tmQ, &args};
   cudaLaunchConfig_t cfg = {};
@@ -1589,6 +1675,20 @@ int pkv_paged_attn_decode(void* out, const void* q, const void* k_cache, const v
                        max_blocks_per_seq, context_lens, nullptr, nullptr, num_seqs, q_len,
                        num_q_heads, num_kv_heads, head_dim, block_size, 0, 1, nullptr, scale,
                        workspace, workspace_bytes, stream);
+}
+
+int pkv_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache,
+                              const void* v_cache, const float* k_scale, const float* v_scale,
+                              int num_blocks, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                              int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, float scale, void* workspace,
+                              size_t workspace_bytes, pkv_stream_t stream) {
+  if (!k_scale || !v_scale) return PKV_EINVAL;
+  return launch_decode(false, out, q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_tables,
+                       max_blocks_per_seq, context_lens, nullptr, nullptr, num_seqs, q_len,
+                       num_q_heads, num_kv_heads, head_dim, block_size, 0, 1, nullptr, scale,
+                       workspace, workspace_bytes, stream, k_scale, v_scale);
 }
 
 int pkv_paged_attn_decode_append(void* out, const void* q, const void* k_new, const void* v_new,

@@ -24,6 +24,7 @@ SYMBOLS = (
     "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes", "pkv_workspace_init",
     "pkv_paged_attn_decode", "pkv_rope_table", "pkv_ring_attn_decode", "pkv_check_tables",
     "pkv_check_slots", "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_decode_append",
+    "pkv_kv_append_fp8", "pkv_paged_attn_decode_fp8",
 )
 
 OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
@@ -89,10 +90,14 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
                                                 i32, i32, i32, f32, P]),
         "pkv_paged_attn_decode_append": (i32, [P, P, P, P, P, P, i32, P, i32, P, i32, i32,
                                                i32, i32, i32, i32, f32, P, sz, P]),
+        "pkv_kv_append_fp8": (i32, [P, P, P, i32, P, P, i32, i32, i32, i32, P, P, P]),
+        "pkv_paged_attn_decode_fp8": (i32, [P, P, P, P, P, P, i32, P, i32, P, i32, i32, i32,
+                                            i32, i32, i32, f32, P, sz, P]),
     }
     for name, (res, args) in sig.items():
-        f = getattr(lib, name)
-        f.restype, f.argtypes = res, args
+        f = getattr(lib, name, None)    # an older build may lack newer entry points
+        if f is not None:
+            f.restype, f.argtypes = res, args
     return lib
 
 
@@ -150,6 +155,15 @@ def kv_append(k, v, slots, k_cache, v_cache, stream=None):
         _stream(stream)))
 
 
+def kv_append_fp8(k, v, slots, k_cache, v_cache, k_scale, v_scale, stream=None):
+    """k, v fp16 [T, Hkv, D]; k_cache, v_cache one layer of uint8 E4M3 codes [NB, Hkv, bs, D];
+    k_scale, v_scale float32 [Hkv] on the device."""
+    nb, hkv, bs, d = k_cache.shape
+    _check("pkv_kv_append_fp8", load().pkv_kv_append_fp8(
+        _p(k), _p(v), _p(slots), slots.numel(), _p(k_cache), _p(v_cache), nb, hkv, d, bs,
+        _p(k_scale), _p(v_scale), _stream(stream)))
+
+
 def copy_blocks(k_cache, v_cache, src, dst, stream=None):
     """k_cache, v_cache [layers, NB, Hkv, bs, D] (or one layer [NB, Hkv, bs, D])."""
     kc = k_cache if k_cache.dim() == 5 else k_cache.unsqueeze(0)
@@ -189,6 +203,20 @@ def paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, scal
         _p(out), _p(q), _p(k_cache), _p(v_cache), nb, _p(block_tables), block_tables.shape[1],
         _p(context_lens), B, q_len, hq, hkv, d, bs, float(scale), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def paged_attn_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                          scale, workspace, stream=None):
+    """paged_attn_decode over an E4M3 cache: uint8 pools [NB, Hkv, bs, D], float32 per-kv-head
+    scales [Hkv] (element value = code * scale)."""
+    B, q_len, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_paged_attn_decode_fp8", load().pkv_paged_attn_decode_fp8(
+        _p(out), _p(q), _p(k_cache), _p(v_cache), _p(k_scale), _p(v_scale), nb,
+        _p(block_tables), block_tables.shape[1], _p(context_lens), B, q_len, hq, hkv, d, bs,
+        float(scale), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return out
 
 
