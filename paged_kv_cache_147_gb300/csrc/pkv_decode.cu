@@ -125,12 +125,12 @@ template <int NCW, int NST, int MT, bool FP8 = false>
 struct Smem {
   static constexpr int kNST = NST;
   // a stage holds one chunk's K and V: fp16 (8 KB) or E4M3 (4 KB: two 16 x 128-byte tiles,
-  // each consumer warp expanding its chunks into an 8 KB fp16 scratch tile of its own)
+  // each consumer warp widening its chunks' V tile into a 4 KB fp16 tile of its own)
   static constexpr int kStage = FP8 ? 2 * kChunk * kD : kStageBytes;
-  static constexpr int kScratch = NST * kStage;        // FP8: NCW x 8 KB fp16 tiles
+  static constexpr int kScratch = NST * kStage;        // FP8: NCW x 4 KB fp16 V tiles
   static constexpr int kQHalf = MT * 2048;            // 16*MT rows x 128 B
   static constexpr int kQBuf = 2 * kQHalf;
-  static constexpr int kQ = kScratch + (FP8 ? NCW * kStageBytes : 0);
+  static constexpr int kQ = kScratch + (FP8 ? NCW * 2 * kHalfBytes : 0);
   // full[NST], empty[NST], qfull[2], qempty[2], sdone[2], sfree[2]
   static constexpr int kBars = kQ + 2 * kQBuf;
   static constexpr int kFlags = kBars + (2 * NST + 8) * 8;  // abort, pending count + units
@@ -479,16 +479,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
   return y;
 }
 
-// Expands one chunk's E4M3 K and V tiles (16 rows x 128 bytes each, 128B-swizzled as the tensor
-// copy lays them out) into fp16 tiles laid out as an fp16 stage is (per tile two 64-column
-// halves of 16 rows x 128 bytes, 128B-swizzled), so that the fp16 fragment loads read them
-// unchanged. One warp: lane-owned 16-byte pieces, 16 codes in, 32 bytes out.
-__device__ __forceinline__ void expand_e4m3_chunk(uint32_t src, uint32_t dst, int lane) {
+// Widens one chunk's E4M3 V tile (16 rows x 128 bytes, 128B-swizzled as the tensor copy lays it
+// out) into an fp16 tile laid out as an fp16 stage's V is (two 64-column halves of 16 rows x
+// 128 bytes, 128B-swizzled), so that the fp16 transposing fragment loads read it unchanged.
+// One warp: lane-owned 16-byte pieces, 16 codes in, 32 bytes out.
+__device__ __forceinline__ void expand_e4m3_tile(uint32_t src, uint32_t dst, int lane) {
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int item = it * 32 + lane;                 // (tile, row, 16-byte piece)
-    const int tile = item >> 7, r = (item >> 3) & 15, c8 = item & 7;
-    const uint4 v = ld_shared_v4(src + tile * 2048 + swz128(r, c8));
+  for (int it = 0; it < 4; ++it) {
+    const int item = it * 32 + lane;                 // (row, 16-byte piece)
+    const int r = item >> 3, c8 = item & 7;
+    const uint4 v = ld_shared_v4(src + swz128(r, c8));
     uint4 lo, hi;
     lo.x = e4m3x2_to_f16x2(v.x & 0xffffu);
     lo.y = e4m3x2_to_f16x2(v.x >> 16);
@@ -499,7 +499,7 @@ __device__ __forceinline__ void expand_e4m3_chunk(uint32_t src, uint32_t dst, in
     hi.z = e4m3x2_to_f16x2(v.w & 0xffffu);
     hi.w = e4m3x2_to_f16x2(v.w >> 16);
     // codes 16 c8 .. 16 c8 + 15 are fp16 columns in half c8 / 4, pieces 2 c8 % 8 and + 1
-    const uint32_t base = dst + tile * 2 * kHalfBytes + (c8 >> 2) * kHalfBytes;
+    const uint32_t base = dst + (c8 >> 2) * kHalfBytes;
     const int cc = (2 * c8) & 7;
     st_shared_v4(base + swz128(r, cc), lo);
     st_shared_v4(base + swz128(r, cc + 1), hi);
@@ -865,14 +865,29 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       // holds rows 2t4 and 2t4 + 1 of the group, keys g and g + 8, dims 16 dt + g (+ 8).
       // Q^T fragments (B operand): rows 0-7 of the query tile
       uint32_t qb0[8], qb1[8];
+      if constexpr (FP8) {
+        // E4M3 keys: thread t4 takes dims 16 s8 + 4 t4 .. + 3 of every 16-dim step as its
+        // fragment columns 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9 (a reordering of the summed
+        // dimension, the same for keys and queries), so that its four key codes are one
+        // 32-bit word of a row
 #pragma unroll
-      for (int s8 = 0; s8 < 8; ++s8) {
-        const int i = lane >> 3;
-        const int row = (i & 1) * 8 + (lane & 7);
-        const int ch = 2 * s8 + (i >> 1);
-        uint32_t unused0, unused1;
-        ldsm_x4(qb + (ch >> 3) * L::kQHalf + swz128(row, ch & 7), qb0[s8], unused0, qb1[s8],
-                unused1);
+        for (int s8 = 0; s8 < 8; ++s8) {
+          const int d0 = 16 * s8 + 4 * t4;
+          const uint2 qq = ld_shared_v2(qb + (d0 >> 6) * L::kQHalf + swz128(g, (d0 & 63) >> 3) +
+                                        (d0 & 7) * 2);
+          qb0[s8] = qq.x;
+          qb1[s8] = qq.y;
+        }
+      } else {
+#pragma unroll
+        for (int s8 = 0; s8 < 8; ++s8) {
+          const int i = lane >> 3;
+          const int row = (i & 1) * 8 + (lane & 7);
+          const int ch = 2 * s8 + (i >> 1);
+          uint32_t unused0, unused1;
+          ldsm_x4(qb + (ch >> 3) * L::kQHalf + swz128(row, ch & 7), qb0[s8], unused0, qb1[s8],
+                  unused1);
+        }
       }
       if (!kHoldQ) {
         __syncwarp();
@@ -896,17 +911,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const int gj = j + jj;
         const int st = gj % NST;
         if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
-        uint32_t stK = sbase + st * L::kStage;
+        const uint32_t stK = sbase + st * L::kStage;
+        uint32_t stV = stK + 2 * kHalfBytes;
         if constexpr (FP8) {
-          // expand into this warp's fp16 tiles (its previous chunk's reads are done), then
-          // free the stage at once
-          stK = sbase + L::kScratch + w * kStageBytes;
+          // widen the V codes into this warp's fp16 tile (its previous chunk's reads are
+          // done); the K codes are read in place below
+          stV = sbase + L::kScratch + w * 2 * kHalfBytes;
           __syncwarp();
-          expand_e4m3_chunk(sbase + st * L::kStage, stK, lane);
+          expand_e4m3_tile(stK + kChunk * kD, stV, lane);
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_empty + st * 8);
         }
-        const uint32_t stV = stK + 2 * kHalfBytes;
         const int c = s.c0 + jj;
         const bool full_chunk = (c + 1) * kChunk <= Lc - a.q_len + 1;
         bool patched = false;
@@ -931,8 +945,24 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         }
         // ---- S^T = K Q^T: K fragments as the A operand (keys g, g + 8), two chains ----
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (FP8) {
+          // keys g and g + 8: one word of four codes each per 16-dim step, widened in registers
 #pragma unroll
-        for (int sp = 0; sp < 4; ++sp) {
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t w0 = ld_shared_u32(stK + swz128(g, ks) + 4 * t4);
+            const uint32_t w1 = ld_shared_u32(stK + swz128(g + 8, ks) + 4 * t4);
+            const uint32_t a0 = e4m3x2_to_f16x2(w0 & 0xffffu), a2 = e4m3x2_to_f16x2(w0 >> 16);
+            const uint32_t a1 = e4m3x2_to_f16x2(w1 & 0xffffu), a3 = e4m3x2_to_f16x2(w1 >> 16);
+            if (ks & 1)
+              mma_16816(sb2, a0, a1, a2, a3, qb0[ks], qb1[ks]);
+            else
+              mma_16816(sa, a0, a1, a2, a3, qb0[ks], qb1[ks]);
+          }
+          __syncwarp();                      // every code of the stage has been read
+          if (lane == 0) mbar_arrive(bar_empty + st * 8);
+        }
+#pragma unroll
+        for (int sp = 0; sp < (FP8 ? 0 : 4); ++sp) {
           uint32_t k0[4], k1[4];   // keys 0-7 and 8-15, dims 32 sp .. 32 sp + 31
           const int ch = 4 * sp + (lane >> 3);
           ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(lane & 7, ch & 7), k0[0], k0[1], k0[2],
@@ -1401,15 +1431,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 // read) and are bound by the consumers' arithmetic: four consumer warps, eight stages.
 constexpr int kNCW = PKV_DECODE_WARPS, kNST = PKV_DECODE_STAGES;
 constexpr int kNCWRing = 4, kNSTRing = 8;
-// The E4M3 cache: 4 KB stages plus an 8 KB fp16 tile per consumer warp, within the shared
-// memory of the fp16 kernels (two CTAs per SM). Widening the codes costs each consumer warp
-// about as much as its mma work, so four consumer warps share the chunks (eight stages, 32 KB
-// of K/V in flight per CTA: half the bytes of the fp16 kernels' chunks).
+// The E4M3 cache: 4 KB stages plus a 4 KB fp16 V tile per consumer warp, within the shared
+// memory of the fp16 kernels (two CTAs per SM). Widening the codes adds to each consumer warp's
+// work, so four consumer warps share the chunks (twelve stages, 48 KB of K/V in flight per CTA).
 #ifndef PKV_FP8_WARPS
 #define PKV_FP8_WARPS 4
 #endif
 #ifndef PKV_FP8_STAGES
-#define PKV_FP8_STAGES 8
+#define PKV_FP8_STAGES 12
 #endif
 constexpr int kNCWFp8 = PKV_FP8_WARPS, kNSTFp8 = PKV_FP8_STAGES;
 
