@@ -58,7 +58,7 @@ def parse_args():
                     help="budget of the CPU-baseline sample")
     ap.add_argument("--kv", choices=["fp16", "fp8"], default="fp16",
                     help="fp8: an E4M3 cache with per-kv-head scales (paged GQA workloads): per "
-                         "layer the FP8 append of the step's rows, then FP8 decode attention")
+                         "layer one launch appends the step's rows as E4M3 and decodes")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers than the workload's (small profiler captures; the "
                          "per-launch figures are unchanged, the step and the L2 note shrink)")
@@ -210,7 +210,7 @@ class Step:
         self.out = torch.empty_like(self.q)
         self.slots = torch.empty(seq.shape[0], dtype=torch.int64, device=dev)
         self.ws = pkv.make_workspace(w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, dev)
-        self.launches_per_step = 2 * Lr + 1 if self.kind == "fp8" else Lr
+        self.launches_per_step = Lr
         if self.kind == "ring":
             self.L = torch.as_tensor(w.context_lens.astype(np.int64), device=dev)
             self.hw = self.L.clone()
@@ -223,13 +223,10 @@ class Step:
         if self.kind == "decode":
             return self.run_decode_only()
         if self.kind == "fp8":
-            p.slot_mapping(self.seq, self.pos, self.bt, w.block_size, out=self.slots)
             for l in range(w.num_layers):
-                p.kv_append_fp8(self.kn[l], self.vn[l], self.slots, self.k[l], self.v[l],
-                                self.ks[l], self.vs[l])
-                p.paged_attn_decode_fp8(self.out[l], self.q[l], self.k[l], self.v[l],
-                                        self.ks[l], self.vs[l], self.bt, self.cl, w.scale,
-                                        self.ws)
+                p.paged_attn_decode_append_fp8(self.out[l], self.q[l], self.kn[l], self.vn[l],
+                                               self.k[l], self.v[l], self.ks[l], self.vs[l],
+                                               self.bt, self.cl, w.scale, self.ws)
             return
         for l in range(w.num_layers):
             if self.kind == "ring":
@@ -276,14 +273,14 @@ class Step:
         if self.kind == "ring":
             return f"CUDA graph: {n} x ring_attn_decode ({self.w.q_len} causal draft queries)"
         if self.kind == "fp8":
-            return (f"CUDA graph: slot_mapping, then {n} x (kv_append_fp8 + "
-                    "paged_attn_decode_fp8)")
+            return (f"CUDA graph: {n} x paged_attn_decode_append_fp8 "
+                    "(slot mapping + E4M3 append + decode, one launch)")
         return (f"CUDA graph: {n} x paged_attn_decode_append "
                 "(slot mapping + KV append + decode, one launch)")
 
     def kernel_note(self) -> str:
         return {"decode": "decode_kernel (paged_attn_decode)",
-                "fp8": "decode_kernel, E4M3 cache (paged_attn_decode_fp8)",
+                "fp8": "decode_kernel, E4M3 cache, fused append (paged_attn_decode_append_fp8)",
                 "ring": "decode_kernel, sink + ring with RoPE on read (ring_attn_decode)"}.get(
             self.kind, "decode_kernel, fused append (paged_attn_decode_append)")
 
@@ -448,8 +445,8 @@ def run_ours(args, w, rank, local_rank, world_size):
     # the step time over its launches (they run back to back, the fused ones each overlapping
     # the previous one's tail). The unfused decode is timed alone as well. For the prefix batch
     # the roofline counts the distinct block rows (the shared prefix once). With the E4M3
-    # cache a layer is an FP8 append plus the decode: launch_us is their sum, and the decode
-    # alone is unfused_decode_launch_us.
+    # cache the fused launch appends and decodes; the decode alone is
+    # unfused_decode_launch_us.
     per_launch = (t_max / args.steps) / w.num_layers
     bytes_launch = (unique_bytes(w) if w.name == "prefix" else bytes_step) / w.num_layers
     peak, peak_kind = load_peaks()

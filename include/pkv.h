@@ -244,6 +244,20 @@ int pkv_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache,
                               int block_size, float scale, void* workspace,
                               size_t workspace_bytes, pkv_stream_t stream);
 
+/* pkv_paged_attn_decode_append over an E4M3 cache: the step's new rows k_new, v_new (fp16, as for
+ * pkv_paged_attn_decode_append) are stored as pkv_kv_append_fp8 stores them (the same codes) and
+ * attended over as pkv_paged_attn_decode_fp8 reads the cache. One launch per layer, with the
+ * early-start contract of pkv_paged_attn_decode_append (k_scale and v_scale are read after the
+ * preceding kernel completes). Requires (num_q_heads / num_kv_heads) * q_len <= 8. */
+int pkv_paged_attn_decode_append_fp8(void* out, const void* q, const void* k_new,
+                                     const void* v_new, void* k_cache, void* v_cache,
+                                     const float* k_scale, const float* v_scale, int num_blocks,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int q_len,
+                                     int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, float scale, void* workspace,
+                                     size_t workspace_bytes, pkv_stream_t stream);
+
 /* ---- host-side validation (debug mode; all arrays are HOST copies) ---------------------------
  * pkv_check_tables: every block-table entry a sequence uses (the first
  * ceil(context_lens[b]/block_size)) is in [0, num_blocks), and 0 <= context_lens[b] <=

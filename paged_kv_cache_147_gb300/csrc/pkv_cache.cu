@@ -92,15 +92,6 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __res
     v_cache[dst] = __ldg(v + src);
 }
 
-// fp32 pair -> E4M3 pair (first value in the low byte): round to nearest even, finite
-// values past 448 saturate.
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
-  uint32_t d;
-  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
-      : "=r"(d) : "f"(lo), "f"(hi));
-  return d;
-}
-
 // FP8 append: thread = 8 consecutive elements of one (token, K|V, kv head) row: 16 fp16 bytes
 // in, each divided by the head's scale in binary32 and rounded to E4M3, 8 bytes out.
 __global__ void kv_append_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
@@ -129,14 +120,8 @@ __global__ void kv_append_fp8_kernel(const uint4* __restrict__ k, const uint4* _
   const int64_t src = (static_cast<int64_t>(t) * num_kv_heads + h) * vecs_per_row + c;
   const uint4 x = __ldg((which ? v : k) + src);
   const float sc = __ldg((which ? v_scale : k_scale) + h);
-  const __half2* hx = reinterpret_cast<const __half2*>(&x);
-  uint32_t q[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(hx[i]);
-    q[i] = f32x2_to_e4m3x2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc));
-  }
-  (which ? v_cache : k_cache)[dst] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+  (which ? v_cache : k_cache)[dst] =
+      make_uint2(f16x4_to_e4m3x4(x.x, x.y, sc), f16x4_to_e4m3x4(x.z, x.w, sc));
 }
 
 // grid.y enumerates (layer, pair, K|V); grid.x strides over the block's 16-byte vectors.

@@ -548,7 +548,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   static_assert(NST % NCW == 0, "pipeline stages must be a multiple of the consumer warps");
   static_assert(!(RING && APPEND), "the ring variant appends through its own slot mapping");
   static_assert(!TR || (MT == 1 && !RING), "the transposed tile is for up to 8 rows, paged");
-  static_assert(!FP8 || (TR && !APPEND), "the E4M3 cache is read by the transposed tile only");
+  static_assert(!FP8 || TR, "the E4M3 cache is read by the transposed tile only");
   // the queries' buffer stays in use for the whole segment when its fragments are not kept in
   // registers, or when it also holds the segment's new K/V rows
   constexpr bool kHoldQ = MT != 1 || APPEND;
@@ -913,14 +913,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
         const uint32_t stK = sbase + st * L::kStage;
         uint32_t stV = stK + 2 * kHalfBytes;
-        if constexpr (FP8) {
-          // widen the V codes into this warp's fp16 tile (its previous chunk's reads are
-          // done); the K codes are read in place below
-          stV = sbase + L::kScratch + w * 2 * kHalfBytes;
-          __syncwarp();
-          expand_e4m3_tile(stK + kChunk * kD, stV, lane);
-          __syncwarp();
-        }
         const int c = s.c0 + jj;
         const bool full_chunk = (c + 1) * kChunk <= Lc - a.q_len + 1;
         bool patched = false;
@@ -928,20 +920,52 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           const int first_new = Lc - a.q_len;
           const int srow = srow_s[st];
           const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
-          const int which = lane >> 4, ch = lane & 15;   // lanes 0-15: K, 16-31: V
-          for (int i = 0; i < a.q_len; ++i) {
-            const int pos = first_new + i;
-            if (pos < c * kChunk || pos >= (c + 1) * kChunk || pos < 0) continue;
-            const int tok = pos - c * kChunk;
-            const uint4 val = ld_shared_v4(nkv + i * 512 + which * 256 + ch * 16);
-            st_shared_v4((which ? stV : stK) + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), val);
-            if (srow >= 0) {
-              __half* pool = which ? a.v_pool : a.k_pool;
-              *reinterpret_cast<uint4*>(pool + (static_cast<int64_t>(srow) + tok) * kD + ch * 8) = val;
+          if constexpr (FP8) {
+            // E4M3 cache: lanes 0-7 quantise a 16-element piece of the new K row, 8-15 of the
+            // V row (divided by the head's scale in binary32, as pkv_kv_append_fp8 does), into
+            // the stage's code tiles and the pool
+            const int which = (lane >> 3) & 1, p = lane & 7;
+            const float sc = __ldg((which ? a.v_scale : a.k_scale) + s.h);
+            for (int i = 0; i < a.q_len; ++i) {
+              const int pos = first_new + i;
+              if (lane >= 16 || pos < c * kChunk || pos >= (c + 1) * kChunk || pos < 0) continue;
+              const int tok = pos - c * kChunk;
+              const uint4 h0 = ld_shared_v4(nkv + i * 512 + which * 256 + p * 32);
+              const uint4 h1 = ld_shared_v4(nkv + i * 512 + which * 256 + p * 32 + 16);
+              const uint4 q8 = make_uint4(f16x4_to_e4m3x4(h0.x, h0.y, sc),
+                                          f16x4_to_e4m3x4(h0.z, h0.w, sc),
+                                          f16x4_to_e4m3x4(h1.x, h1.y, sc),
+                                          f16x4_to_e4m3x4(h1.z, h1.w, sc));
+              st_shared_v4(stK + which * (kChunk * kD) + swz128(tok, p), q8);
+              if (srow >= 0) {
+                uint8_t* pool = reinterpret_cast<uint8_t*>(which ? a.v_pool : a.k_pool);
+                *reinterpret_cast<uint4*>(pool + (static_cast<int64_t>(srow) + tok) * kD + p * 16) = q8;
+              }
+            }
+          } else {
+            const int which = lane >> 4, ch = lane & 15;   // lanes 0-15: K, 16-31: V
+            for (int i = 0; i < a.q_len; ++i) {
+              const int pos = first_new + i;
+              if (pos < c * kChunk || pos >= (c + 1) * kChunk || pos < 0) continue;
+              const int tok = pos - c * kChunk;
+              const uint4 val = ld_shared_v4(nkv + i * 512 + which * 256 + ch * 16);
+              st_shared_v4((which ? stV : stK) + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), val);
+              if (srow >= 0) {
+                __half* pool = which ? a.v_pool : a.k_pool;
+                *reinterpret_cast<uint4*>(pool + (static_cast<int64_t>(srow) + tok) * kD + ch * 8) = val;
+              }
             }
           }
           __syncwarp();
           patched = true;
+        }
+        if constexpr (FP8) {
+          // widen the V codes into this warp's fp16 tile (its previous chunk's reads are
+          // done); the K codes are read in place below
+          stV = sbase + L::kScratch + w * 2 * kHalfBytes;
+          __syncwarp();
+          expand_e4m3_tile(stK + kChunk * kD, stV, lane);
+          __syncwarp();
         }
         // ---- S^T = K Q^T: K fragments as the A operand (keys g, g + 8), two chains ----
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -958,6 +982,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             else
               mma_16816(sa, a0, a1, a2, a3, qb0[ks], qb1[ks]);
           }
+          if (APPEND && patched) fence_proxy_async_smem();
           __syncwarp();                      // every code of the stage has been read
           if (lane == 0) mbar_arrive(bar_empty + st * 8);
         }
@@ -1545,7 +1570,7 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   const bool append = k_new != nullptr;
   if (append && (ring || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
   const bool fp8 = k_scale != nullptr;
-  if (fp8 && (ring || append || !v_scale || G * q_len > 8)) return PKV_EINVAL;
+  if (fp8 && (ring || !v_scale || G * q_len > 8)) return PKV_EINVAL;
   if (ring) {
     if (!logical_len || !high_water || !rope || sink < 0 || window < 1) return PKV_EINVAL;
     if ((sink + window + block_size - 1) / block_size > max_blocks) return PKV_EINVAL;
@@ -1564,7 +1589,8 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   const int mt = R <= 16 ? 1 : 2;
   // up to 8 rows per unit (GQA groups of 6-8 at one query token): the transposed tile
   const bool tr = !ring && R <= 8;
-  Variant v = fp8      ? variant<1, false, false, true, true>()
+  Variant v = fp8      ? (append ? variant<1, false, true, true, true>()
+                                 : variant<1, false, false, true, true>())
               : ring   ? (mt == 1 ? variant<1, true, false>() : variant<2, true, false>())
               : append ? (tr ? variant<1, false, true, true>()
                              : mt == 1 ? variant<1, false, true>() : variant<2, false, true>())
@@ -1704,6 +1730,22 @@ int pkv_paged_attn_decode(void* out, const void* q, const void* k_cache, const v
                        max_blocks_per_seq, context_lens, nullptr, nullptr, num_seqs, q_len,
                        num_q_heads, num_kv_heads, head_dim, block_size, 0, 1, nullptr, scale,
                        workspace, workspace_bytes, stream);
+}
+
+int pkv_paged_attn_decode_append_fp8(void* out, const void* q, const void* k_new,
+                                     const void* v_new, void* k_cache, void* v_cache,
+                                     const float* k_scale, const float* v_scale, int num_blocks,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int q_len,
+                                     int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, float scale, void* workspace,
+                                     size_t workspace_bytes, pkv_stream_t stream) {
+  if (!k_scale || !v_scale || (num_seqs > 0 && (!k_new || !v_new))) return PKV_EINVAL;
+  return launch_decode(false, out, q, num_seqs > 0 ? k_new : nullptr, v_new, k_cache, v_cache,
+                       num_blocks, block_tables, max_blocks_per_seq, context_lens, nullptr,
+                       nullptr, num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
+                       block_size, 0, 1, nullptr, scale, workspace, workspace_bytes, stream,
+                       k_scale, v_scale);
 }
 
 int pkv_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache,

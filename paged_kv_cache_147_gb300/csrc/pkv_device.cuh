@@ -122,6 +122,24 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
   return v;
 }
 
+// fp32 pair -> E4M3 pair (first value in the low byte): round to nearest even, finite values
+// past 448 saturate to +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+
+// Four fp16 values (two packed pairs) divided by `scale` in binary32 -> four E4M3 codes, the
+// first in the low byte.
+__device__ __forceinline__ uint32_t f16x4_to_e4m3x4(uint32_t h01, uint32_t h23, float scale) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  return f32x2_to_e4m3x2(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale)) |
+         (f32x2_to_e4m3x2(__fdiv_rn(b.x, scale), __fdiv_rn(b.y, scale)) << 16);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)

@@ -24,7 +24,7 @@ SYMBOLS = (
     "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes", "pkv_workspace_init",
     "pkv_paged_attn_decode", "pkv_rope_table", "pkv_ring_attn_decode", "pkv_check_tables",
     "pkv_check_slots", "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_decode_append",
-    "pkv_kv_append_fp8", "pkv_paged_attn_decode_fp8",
+    "pkv_kv_append_fp8", "pkv_paged_attn_decode_fp8", "pkv_paged_attn_decode_append_fp8",
 )
 
 OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
@@ -93,6 +93,8 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
         "pkv_kv_append_fp8": (i32, [P, P, P, i32, P, P, i32, i32, i32, i32, P, P, P]),
         "pkv_paged_attn_decode_fp8": (i32, [P, P, P, P, P, P, i32, P, i32, P, i32, i32, i32,
                                             i32, i32, i32, f32, P, sz, P]),
+        "pkv_paged_attn_decode_append_fp8": (i32, [P, P, P, P, P, P, P, P, i32, P, i32, P, i32,
+                                                   i32, i32, i32, i32, i32, f32, P, sz, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name, None)    # an older build may lack newer entry points
@@ -216,6 +218,20 @@ def paged_attn_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tabl
         _p(out), _p(q), _p(k_cache), _p(v_cache), _p(k_scale), _p(v_scale), nb,
         _p(block_tables), block_tables.shape[1], _p(context_lens), B, q_len, hq, hkv, d, bs,
         float(scale), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return out
+
+
+def paged_attn_decode_append_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                 block_tables, context_lens, scale, workspace, stream=None):
+    """paged_attn_decode_append over an E4M3 cache: the new fp16 rows are stored as
+    kv_append_fp8 stores them and attended over with the rest of the cache."""
+    B, q_len, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_paged_attn_decode_append_fp8", load().pkv_paged_attn_decode_append_fp8(
+        _p(out), _p(q), _p(k_new), _p(v_new), _p(k_cache), _p(v_cache), _p(k_scale),
+        _p(v_scale), nb, _p(block_tables), block_tables.shape[1], _p(context_lens), B, q_len, hq,
+        hkv, d, bs, float(scale), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
     return out
 

@@ -139,3 +139,63 @@ def test_decode_fp8_is_deterministic_and_rejects_wide_groups():
     with pytest.raises(pkv.PkvError) as e:
         _gpu_decode_fp8(k8, v8, ks, vs, tables, lens, q, 0.1)
     assert e.value.status == pkv.EINVAL
+
+
+def _new_slots(tables, lens, q_len, bs):
+    slots = []
+    for b, L in enumerate(lens):
+        for i in range(q_len):
+            pos = int(L) - q_len + i
+            slots.append(-1 if pos < 0 else int(tables[b, pos // bs]) * bs + pos % bs)
+    return np.asarray(slots, np.int64)
+
+
+@pytest.mark.parametrize("lens,bs,hq,hkv,q_len", [
+    ([38, 101], 16, 12, 2, 1),                           # the tiny batch
+    ([33, 16, 2, 100], 16, 8, 4, 2),                     # causal pairs, new rows across blocks
+    ([64, 5, 31, 4], 16, 4, 4, 4),                       # MHA drafts (R = 4)
+    ([500, 70, 1], 64, 16, 2, 1),                        # 64-token blocks
+])
+def test_fused_append_decode_fp8_matches_oracle(lens, bs, hq, hkv, q_len):
+    k8, v8, ks, vs, tables, lens, q = _fp8_case(lens, bs, hq, hkv, q_len, seed=len(lens) * 7 + q_len)
+    rng = np.random.default_rng(99)
+    kn = rng.standard_normal((len(lens) * q_len, hkv, 128)).astype(np.float16)
+    vn = rng.standard_normal((len(lens) * q_len, hkv, 128)).astype(np.float16)
+    k8_d, v8_d = _dev(k8), _dev(v8)
+    qd = _dev(q)
+    out = torch.empty_like(qd)
+    ws = pkv.make_workspace(q.shape[0], q_len, hq, hkv)
+    scale = 1 / math.sqrt(128)
+    pkv.paged_attn_decode_append_fp8(out, qd, _dev(kn), _dev(vn), k8_d, v8_d, _dev(ks), _dev(vs),
+                                     _dev(tables, torch.int32), _dev(lens, torch.int32), scale, ws)
+    torch.cuda.synchronize()
+    assert pkv.device_error(clear=True) == 0
+    oracle.kv_append_fp8(kn, vn, _new_slots(tables, lens, q_len, bs), k8, v8, bs, ks, vs)
+    assert np.array_equal(k8_d.cpu().numpy(), k8) and np.array_equal(v8_d.cpu().numpy(), v8)
+    ref = oracle.paged_attention_fp8(q, k8, v8, ks, vs, tables, lens, bs, scale)
+    assert_attn_close(out, ref, f"fp8 fused lens={list(lens[:4])} q_len={q_len}")
+
+
+def test_fused_append_decode_fp8_on_the_edge_shape():
+    w = workloads.edge_1p1b()
+    rng = np.random.default_rng(8)
+    kf = rng.standard_normal((w.num_blocks, w.num_kv_heads, w.block_size, 128), np.float32)
+    vf = rng.standard_normal((w.num_blocks, w.num_kv_heads, w.block_size, 128), np.float32)
+    ks = (np.abs(kf).max(axis=(0, 2, 3)) / 448.0).astype(np.float32)
+    vs = (np.abs(vf).max(axis=(0, 2, 3)) / 448.0).astype(np.float32)
+    k8, v8 = _quantise(kf, ks), _quantise(vf, vs)
+    q = w.query(0, DEV)
+    kn, vn = w.new_kv(0, DEV)
+    k8_d, v8_d = _dev(k8), _dev(v8)
+    out = torch.empty_like(q)
+    ws = pkv.make_workspace(w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads)
+    pkv.paged_attn_decode_append_fp8(out, q, kn, vn, k8_d, v8_d, _dev(ks), _dev(vs),
+                                     _dev(w.block_tables, torch.int32),
+                                     _dev(w.context_lens, torch.int32), w.scale, ws)
+    torch.cuda.synchronize()
+    slots = _new_slots(w.block_tables, w.context_lens, w.q_len, w.block_size)
+    oracle.kv_append_fp8(f16_host(kn), f16_host(vn), slots, k8, v8, w.block_size, ks, vs)
+    assert np.array_equal(k8_d.cpu().numpy(), k8) and np.array_equal(v8_d.cpu().numpy(), v8)
+    ref = oracle.paged_attention_fp8(f16_host(q), k8, v8, ks, vs, w.block_tables, w.context_lens,
+                                     w.block_size, w.scale)
+    assert_attn_close(out, ref, "fp8 fused edge_1p1b")
