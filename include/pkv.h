@@ -258,6 +258,55 @@ int pkv_paged_attn_decode_append_fp8(void* out, const void* q, const void* k_new
                                      int block_size, float scale, void* workspace,
                                      size_t workspace_bytes, pkv_stream_t stream);
 
+/* ---- host block pool ------------------------------------------------------------------------
+ * The host side of paging ([OLLAMA] §三 KV Cache内存管理的工程实现, and its copy-on-write
+ * paragraph): num_blocks physical blocks of block_size tokens, a FIFO free list, a reference
+ * count per block, and a prefix index so that sequences whose prompts begin with the same full
+ * blocks of token ids share those blocks. It hands out the block tables and the copy pairs the
+ * CUDA entry points take; it owns no device memory. All arrays are HOST int32; every call
+ * locks the pool (one pool may serve several threads). Errors: PKV_EINVAL (bad arguments,
+ * a table entry that is not a held block, an output array too small), PKV_ENOSPC (not enough
+ * blocks even after reclaiming warm ones); a failed call changes nothing.
+ *
+ * Prefix index: full blocks only, keyed by 64-bit FNV-1a (offset basis 0xcbf29ce484222325,
+ * prime 0x100000001b3, each token id xor-ed in as a 32-bit value) over the whole prefix up to
+ * the block's last token (a hash chain); a candidate is reused only if its token ids and the
+ * block before it match (hash_bits < 64 truncates the key, for tests of that check).
+ *
+ * pkv_pool_allocate: reuses the indexed blocks that match the prompt's leading full blocks
+ * (reference +1; *reused of them), then takes ceil((max(max_tokens, n_tokens) - reused *
+ * block_size) / block_size) blocks from the free list (reference 1) and indexes the new full
+ * prompt blocks. table[0 .. *n_blocks) receives the sequence's block table.
+ * pkv_pool_warm: indexes a prompt's full blocks without holding them (reference 0): they stay
+ * out of the free list until reused or reclaimed.
+ * pkv_pool_release: reference -1 per block; at 0 a block leaves the index and goes to the back
+ * of the free list.
+ * pkv_pool_fork: reference +1 per block (a child that shares the parent's table).
+ * pkv_pool_append: makes room for tokens [length, length + n_new) of the sequence: a block past
+ * the table is taken from the pool; a block the sequence shares with others (reference > 1) is
+ * replaced by a fresh one and the pair (copy_src[i], copy_dst[i]) returned, to be copied with
+ * pkv_copy_blocks before the new rows are written (copy-on-write). table / *n_blocks are
+ * updated in place (capacity table_cap). With all_tokens (the sequence's token ids through
+ * length + n_new) the blocks the append fills are indexed when the block before them is.
+ * When the free list is short, warm blocks are reclaimed oldest allocation first; blocks a
+ * sequence holds never are. */
+typedef struct pkv_block_pool pkv_block_pool;
+int pkv_pool_create(int num_blocks, int block_size, int hash_bits, pkv_block_pool** out);
+void pkv_pool_destroy(pkv_block_pool* pool);
+int pkv_pool_allocate(pkv_block_pool* pool, const int32_t* tokens, int n_tokens, int max_tokens,
+                      int32_t* table, int table_cap, int* n_blocks, int* reused);
+int pkv_pool_warm(pkv_block_pool* pool, const int32_t* tokens, int n_tokens);
+int pkv_pool_release(pkv_block_pool* pool, const int32_t* table, int n_blocks);
+int pkv_pool_fork(pkv_block_pool* pool, const int32_t* table, int n_blocks);
+int pkv_pool_append(pkv_block_pool* pool, int32_t* table, int* n_blocks, int table_cap,
+                    int length, int n_new, const int32_t* all_tokens, int32_t* copy_src,
+                    int32_t* copy_dst, int copy_cap, int* n_copies);
+/* Counts: blocks, held blocks, blocks held more than once, free-list length, warm blocks. */
+int pkv_pool_stats(pkv_block_pool* pool, int* total, int* used, int* shared, int* free_blocks,
+                   int* warm);
+/* A block's reference count (or PKV_EINVAL). */
+int pkv_pool_refcount(pkv_block_pool* pool, int block);
+
 /* ---- host-side validation (debug mode; all arrays are HOST copies) ---------------------------
  * pkv_check_tables: every block-table entry a sequence uses (the first
  * ceil(context_lens[b]/block_size)) is in [0, num_blocks), and 0 <= context_lens[b] <=

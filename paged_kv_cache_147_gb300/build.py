@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkv.so")
-SOURCES = ["pkv_decode.cu", "pkv_cache.cu", "pkv_host.cu"]
+SOURCES = ["pkv_decode.cu", "pkv_cache.cu", "pkv_host.cu", "pkv_blocks.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-diag-suppress", "177"]
@@ -47,7 +47,7 @@ def build(force: bool = False, verbose: bool = False, defines=(), out: str | Non
     os.makedirs(bdir, exist_ok=True)
     procs = []
     for src in SOURCES:
-        obj = os.path.join(bdir, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *[f"-D{d}" for d in defines], "-c",
                os.path.join(CSRC, src), "-o", obj]
         procs.append((src, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE,

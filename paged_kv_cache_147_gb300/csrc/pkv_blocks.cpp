@@ -1,0 +1,304 @@
+// pkv_blocks.cpp -- the host KV block pool: fixed-size blocks, a FIFO free list, reference
+// counts, a prefix index of full blocks keyed by an FNV-1a hash chain over token ids, and
+// copy-on-write of shared blocks before an append (the Ollama memory-management page, §三 KV
+// Cache内存管理的工程实现 and its copy-on-write paragraph). It produces the block tables and
+// the copy pairs that the CUDA entry points take (pkv_copy_blocks, the slot mapping, decode).
+//
+// Readings of the page (it leaves them open): a block's index key is the FNV-1a state after
+// its last token continued from its parent block's (a chain over the whole prefix); only full
+// blocks are indexed; a candidate is accepted only if its token ids and its parent block match
+// (the token-level verification the page asks for against collisions); releasing the last
+// reference frees a block and removes it from the index; warm() indexes a prompt's blocks with
+// no reference (the page's pre-warmed system prompt); when the free list is short, indexed
+// unreferenced blocks are reclaimed oldest allocation first, and referenced blocks never are.
+#include <algorithm>
+#include <cstdint>
+#include <deque>
+#include <mutex>
+#include <new>
+#include <unordered_map>
+#include <utility>
+#include <vector>
+
+#include "../../include/pkv.h"
+
+struct pkv_block_pool {
+  int nb = 0, bs = 0;
+  uint64_t mask = ~0ull;
+  std::vector<int> ref, parent;
+  std::vector<uint8_t> indexed;
+  std::vector<uint64_t> key, chain;
+  std::vector<int64_t> stamp;
+  std::vector<std::vector<int32_t>> toks;
+  std::deque<int> free_list;
+  std::unordered_map<uint64_t, std::vector<int>> index;   // key -> blocks, registration order
+  int64_t clock = 0;
+  std::mutex mu;
+};
+
+namespace {
+
+constexpr uint64_t kFnvOffset = 0xcbf29ce484222325ull;
+constexpr uint64_t kFnvPrime = 0x100000001b3ull;
+
+uint64_t fnv1a(const int32_t* t, int n, uint64_t h) {
+  for (int i = 0; i < n; ++i) {
+    h ^= static_cast<uint64_t>(static_cast<uint32_t>(t[i]));
+    h *= kFnvPrime;
+  }
+  return h;
+}
+
+void unindex(pkv_block_pool* p, int b) {
+  if (!p->indexed[b]) return;
+  auto it = p->index.find(p->key[b]);
+  if (it != p->index.end()) {
+    auto& v = it->second;
+    v.erase(std::find(v.begin(), v.end(), b));
+    if (v.empty()) p->index.erase(it);
+  }
+  p->indexed[b] = 0;
+  p->toks[b].clear();
+}
+
+void index_block(pkv_block_pool* p, int b, int parent, uint64_t chain, const int32_t* t) {
+  p->indexed[b] = 1;
+  p->key[b] = chain & p->mask;
+  p->chain[b] = chain;
+  p->parent[b] = parent;
+  p->toks[b].assign(t, t + p->bs);
+  p->index[p->key[b]].push_back(b);
+}
+
+int match(pkv_block_pool* p, int parent, uint64_t chain, const int32_t* t) {
+  auto it = p->index.find(chain & p->mask);
+  if (it == p->index.end()) return -1;
+  for (int b : it->second)
+    if (p->parent[b] == parent && std::equal(t, t + p->bs, p->toks[b].begin())) return b;
+  return -1;
+}
+
+// Takes n blocks from the front of the free list, first reclaiming indexed unreferenced
+// blocks (oldest allocation first) if it is short. All or nothing.
+bool take(pkv_block_pool* p, int n, std::vector<int>& out) {
+  if (static_cast<int>(p->free_list.size()) < n) {
+    std::vector<std::pair<int64_t, int>> warm;
+    for (int b = 0; b < p->nb; ++b)
+      if (p->ref[b] == 0 && p->indexed[b]) warm.emplace_back(p->stamp[b], b);
+    const int need = n - static_cast<int>(p->free_list.size());
+    if (static_cast<int>(warm.size()) < need) return false;
+    std::sort(warm.begin(), warm.end());
+    for (int i = 0; i < need; ++i) {
+      unindex(p, warm[i].second);
+      p->free_list.push_back(warm[i].second);
+    }
+  }
+  for (int i = 0; i < n; ++i) {
+    const int b = p->free_list.front();
+    p->free_list.pop_front();
+    p->stamp[b] = ++p->clock;
+    out.push_back(b);
+  }
+  return true;
+}
+
+bool valid_table(const pkv_block_pool* p, const int32_t* table, int n) {
+  if (n < 0 || (n > 0 && !table)) return false;
+  for (int i = 0; i < n; ++i)
+    if (table[i] < 0 || table[i] >= p->nb || p->ref[table[i]] < 1) return false;
+  return true;
+}
+
+// allocate without locking; refs of the matched prefix are taken before new blocks
+int allocate_locked(pkv_block_pool* p, const int32_t* tokens, int n_tokens, int max_tokens,
+                    int32_t* table, int table_cap, int* n_blocks, int* reused) {
+  const int bs = p->bs;
+  if (max_tokens < n_tokens) max_tokens = n_tokens;
+  std::vector<int> got;
+  int parent = -1, pos = 0;
+  uint64_t h = kFnvOffset;
+  while (pos + bs <= n_tokens) {
+    const uint64_t h2 = fnv1a(tokens + pos, bs, h);
+    const int b = match(p, parent, h2, tokens + pos);
+    if (b < 0) break;
+    got.push_back(b);
+    parent = b;
+    h = h2;
+    pos += bs;
+  }
+  const int n_reused = static_cast<int>(got.size());
+  const int need = (max_tokens - pos + bs - 1) / bs;
+  if (n_reused + need > table_cap) return PKV_EINVAL;
+  for (int b : got) ++p->ref[b];
+  std::vector<int> fresh;
+  if (!take(p, need, fresh)) {
+    for (int b : got) --p->ref[b];
+    return PKV_ENOSPC;
+  }
+  for (int b : fresh) {
+    p->ref[b] = 1;
+    if (pos + bs <= n_tokens) {
+      const uint64_t h2 = fnv1a(tokens + pos, bs, h);
+      index_block(p, b, parent, h2, tokens + pos);
+      parent = b;
+      h = h2;
+    }
+    pos += bs;
+    got.push_back(b);
+  }
+  for (size_t i = 0; i < got.size(); ++i) table[i] = got[i];
+  *n_blocks = static_cast<int>(got.size());
+  if (reused) *reused = n_reused;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_pool_create(int num_blocks, int block_size, int hash_bits, pkv_block_pool** out) {
+  if (!out || num_blocks < 1 || block_size < 1 || hash_bits < 1 || hash_bits > 64)
+    return PKV_EINVAL;
+  auto* p = new (std::nothrow) pkv_block_pool;
+  if (!p) return PKV_ENOSPC;
+  p->nb = num_blocks;
+  p->bs = block_size;
+  p->mask = hash_bits >= 64 ? ~0ull : ((1ull << hash_bits) - 1);
+  p->ref.assign(num_blocks, 0);
+  p->parent.assign(num_blocks, -1);
+  p->indexed.assign(num_blocks, 0);
+  p->key.assign(num_blocks, 0);
+  p->chain.assign(num_blocks, 0);
+  p->stamp.assign(num_blocks, 0);
+  p->toks.assign(num_blocks, {});
+  for (int b = 0; b < num_blocks; ++b) p->free_list.push_back(b);
+  *out = p;
+  return PKV_OK;
+}
+
+void pkv_pool_destroy(pkv_block_pool* pool) { delete pool; }
+
+int pkv_pool_allocate(pkv_block_pool* pool, const int32_t* tokens, int n_tokens, int max_tokens,
+                      int32_t* table, int table_cap, int* n_blocks, int* reused) {
+  if (!pool || n_tokens < 0 || (n_tokens > 0 && !tokens) || !table || !n_blocks ||
+      table_cap < 0)
+    return PKV_EINVAL;
+  std::lock_guard<std::mutex> lock(pool->mu);
+  return allocate_locked(pool, tokens, n_tokens, max_tokens, table, table_cap, n_blocks, reused);
+}
+
+int pkv_pool_warm(pkv_block_pool* pool, const int32_t* tokens, int n_tokens) {
+  if (!pool || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lock(pool->mu);
+  const int full = (n_tokens / pool->bs) * pool->bs;
+  std::vector<int32_t> table(full / pool->bs + 1);
+  int n = 0;
+  const int st = allocate_locked(pool, tokens, full, full, table.data(),
+                                 static_cast<int>(table.size()), &n, nullptr);
+  if (st != PKV_OK) return st;
+  for (int i = 0; i < n; ++i) --pool->ref[table[i]];
+  return PKV_OK;
+}
+
+int pkv_pool_release(pkv_block_pool* pool, const int32_t* table, int n_blocks) {
+  if (!pool) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lock(pool->mu);
+  if (!valid_table(pool, table, n_blocks)) return PKV_EINVAL;
+  for (int i = 0; i < n_blocks; ++i) {
+    const int b = table[i];
+    if (--pool->ref[b] == 0) {
+      unindex(pool, b);
+      pool->free_list.push_back(b);
+    }
+  }
+  return PKV_OK;
+}
+
+int pkv_pool_fork(pkv_block_pool* pool, const int32_t* table, int n_blocks) {
+  if (!pool) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lock(pool->mu);
+  if (!valid_table(pool, table, n_blocks)) return PKV_EINVAL;
+  for (int i = 0; i < n_blocks; ++i) ++pool->ref[table[i]];
+  return PKV_OK;
+}
+
+int pkv_pool_append(pkv_block_pool* pool, int32_t* table, int* n_blocks, int table_cap,
+                    int length, int n_new, const int32_t* all_tokens, int32_t* copy_src,
+                    int32_t* copy_dst, int copy_cap, int* n_copies) {
+  if (!pool || !table || !n_blocks || !n_copies || length < 0 || n_new < 0 || copy_cap < 0 ||
+      (copy_cap > 0 && (!copy_src || !copy_dst)))
+    return PKV_EINVAL;
+  std::lock_guard<std::mutex> lock(pool->mu);
+  const int bs = pool->bs;
+  const int nb0 = *n_blocks;
+  if (!valid_table(pool, table, nb0) || nb0 > table_cap) return PKV_EINVAL;
+  *n_copies = 0;
+  if (n_new == 0) return PKV_OK;
+  const int first = length / bs, last = (length + n_new - 1) / bs;
+  if (first > nb0 || last + 1 > table_cap) return PKV_EINVAL;
+  // count the blocks needed first: all or nothing
+  int need = 0, copies = 0;
+  for (int j = first; j <= last; ++j) {
+    if (j >= nb0) ++need;
+    else if (pool->ref[table[j]] > 1) { ++need; ++copies; }
+  }
+  if (copies > copy_cap) return PKV_EINVAL;
+  std::vector<int> fresh;
+  if (!take(pool, need, fresh)) return PKV_ENOSPC;
+  int used = 0, nb = nb0;
+  for (int j = first; j <= last; ++j) {
+    if (j < nb0 && pool->ref[table[j]] > 1) {
+      const int d = fresh[used++];
+      pool->ref[d] = 1;
+      --pool->ref[table[j]];
+      copy_src[*n_copies] = table[j];
+      copy_dst[*n_copies] = d;
+      ++*n_copies;
+      table[j] = d;
+    } else if (j >= nb0) {
+      const int d = fresh[used++];
+      pool->ref[d] = 1;
+      table[nb++] = d;
+    }
+  }
+  *n_blocks = nb;
+  // index the blocks this append filled, when their parent is indexed
+  if (all_tokens) {
+    for (int j = length / bs; j < (length + n_new) / bs; ++j) {
+      const int b = table[j];
+      if (pool->indexed[b]) continue;
+      const int parent = j > 0 ? table[j - 1] : -1;
+      if (j > 0 && !pool->indexed[parent]) continue;
+      const uint64_t h = j > 0 ? pool->chain[parent] : kFnvOffset;
+      index_block(pool, b, parent, fnv1a(all_tokens + static_cast<int64_t>(j) * bs, bs, h),
+                  all_tokens + static_cast<int64_t>(j) * bs);
+    }
+  }
+  return PKV_OK;
+}
+
+int pkv_pool_stats(pkv_block_pool* pool, int* total, int* used, int* shared, int* free_blocks,
+                   int* warm) {
+  if (!pool) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lock(pool->mu);
+  int u = 0, s = 0, w = 0;
+  for (int b = 0; b < pool->nb; ++b) {
+    u += pool->ref[b] > 0;
+    s += pool->ref[b] > 1;
+    w += pool->ref[b] == 0 && pool->indexed[b];
+  }
+  if (total) *total = pool->nb;
+  if (used) *used = u;
+  if (shared) *shared = s;
+  if (free_blocks) *free_blocks = static_cast<int>(pool->free_list.size());
+  if (warm) *warm = w;
+  return PKV_OK;
+}
+
+int pkv_pool_refcount(pkv_block_pool* pool, int block) {
+  if (!pool || block < 0 || block >= pool->nb) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lock(pool->mu);
+  return pool->ref[block];
+}
+
+}  // extern "C"

@@ -12,6 +12,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -25,6 +26,9 @@ SYMBOLS = (
     "pkv_paged_attn_decode", "pkv_rope_table", "pkv_ring_attn_decode", "pkv_check_tables",
     "pkv_check_slots", "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_decode_append",
     "pkv_kv_append_fp8", "pkv_paged_attn_decode_fp8", "pkv_paged_attn_decode_append_fp8",
+    "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocate", "pkv_pool_warm",
+    "pkv_pool_release", "pkv_pool_fork", "pkv_pool_append", "pkv_pool_stats",
+    "pkv_pool_refcount",
 )
 
 OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
@@ -95,6 +99,15 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
                                             i32, i32, i32, f32, P, sz, P]),
         "pkv_paged_attn_decode_append_fp8": (i32, [P, P, P, P, P, P, P, P, i32, P, i32, P, i32,
                                                    i32, i32, i32, i32, i32, f32, P, sz, P]),
+        "pkv_pool_create": (i32, [i32, i32, i32, P]),
+        "pkv_pool_destroy": (None, [P]),
+        "pkv_pool_allocate": (i32, [P, P, i32, i32, P, i32, P, P]),
+        "pkv_pool_warm": (i32, [P, P, i32]),
+        "pkv_pool_release": (i32, [P, P, i32]),
+        "pkv_pool_fork": (i32, [P, P, i32]),
+        "pkv_pool_append": (i32, [P, P, P, i32, i32, i32, P, P, P, i32, P]),
+        "pkv_pool_stats": (i32, [P, P, P, P, P, P]),
+        "pkv_pool_refcount": (i32, [P, i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name, None)    # an older build may lack newer entry points
@@ -303,3 +316,82 @@ def check_slots(slots, num_blocks, block_size) -> int | None:
         return bad.value
     _check("pkv_check_slots", st)
     return None
+
+
+# ------------------------------------------------------------------------------ host block pool
+class BlockPool:
+    """The library's host block pool (pkv_pool_*): block tables with prefix sharing, reference
+    counts and copy-on-write pairs for pkv_copy_blocks. Tables are int32 numpy arrays."""
+
+    def __init__(self, num_blocks: int, block_size: int, hash_bits: int = 64):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check("pkv_pool_create", self._lib.pkv_pool_create(num_blocks, block_size, hash_bits,
+                                                             ctypes.byref(h)))
+        self._h, self.num_blocks, self.block_size = h, num_blocks, block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pkv_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _i32(a):
+        return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+    def allocate(self, tokens, max_tokens=None, table_cap=None):
+        """-> (table, reused): the sequence's blocks and how many were shared."""
+        t = self._i32(tokens)
+        mt = len(t) if max_tokens is None else int(max_tokens)
+        cap = table_cap or (max(mt, len(t)) // self.block_size + 2)
+        table = np.empty(cap, np.int32)
+        n, reused = ctypes.c_int(0), ctypes.c_int(0)
+        _check("pkv_pool_allocate", self._lib.pkv_pool_allocate(
+            self._h, t.ctypes.data, len(t), mt, table.ctypes.data, cap, ctypes.byref(n),
+            ctypes.byref(reused)))
+        return table[:n.value].copy(), reused.value
+
+    def warm(self, tokens):
+        t = self._i32(tokens)
+        _check("pkv_pool_warm", self._lib.pkv_pool_warm(self._h, t.ctypes.data, len(t)))
+
+    def release(self, table):
+        t = self._i32(table)
+        _check("pkv_pool_release", self._lib.pkv_pool_release(self._h, t.ctypes.data, len(t)))
+
+    def fork(self, table):
+        t = self._i32(table)
+        _check("pkv_pool_fork", self._lib.pkv_pool_fork(self._h, t.ctypes.data, len(t)))
+        return t.copy()
+
+    def append(self, table, length, n_new, all_tokens=None):
+        """-> (table, copies): copies is an int32 [n, 2] array of (src, dst) block pairs."""
+        cap = (length + n_new) // self.block_size + 2
+        t = np.empty(max(cap, len(table)), np.int32)
+        t[:len(table)] = table
+        n = ctypes.c_int(len(table))
+        src, dst = np.empty(cap, np.int32), np.empty(cap, np.int32)
+        nc = ctypes.c_int(0)
+        at = None if all_tokens is None else self._i32(all_tokens)
+        _check("pkv_pool_append", self._lib.pkv_pool_append(
+            self._h, t.ctypes.data, ctypes.byref(n), len(t), int(length), int(n_new),
+            None if at is None else at.ctypes.data, src.ctypes.data, dst.ctypes.data, cap,
+            ctypes.byref(nc)))
+        return t[:n.value].copy(), np.stack([src[:nc.value], dst[:nc.value]], axis=1)
+
+    def stats(self) -> dict:
+        v = [ctypes.c_int(0) for _ in range(5)]
+        _check("pkv_pool_stats", self._lib.pkv_pool_stats(self._h, *[ctypes.byref(x) for x in v]))
+        return dict(zip(("total", "used", "shared", "free", "warm"), (x.value for x in v)))
+
+    def refcount(self, block: int) -> int:
+        r = self._lib.pkv_pool_refcount(self._h, int(block))
+        if r < 0:
+            raise PkvError("pkv_pool_refcount", r)
+        return r
