@@ -62,6 +62,7 @@ typedef void* pkv_stream_t;
 #define PKV_DEVERR_TIMEOUT 8u    /* an in-kernel pipeline wait ran past its iteration limit */
 #define PKV_DEVERR_SEQ 16u       /* a sequence id outside [0, num_seqs) */
 #define PKV_DEVERR_POSITION 32u  /* a position past the sequence's block table */
+#define PKV_DEVERR_TOKEN 64u     /* a draft token id outside [0, vocab) (treated as rejected) */
 
 /* Library version (major*10000 + minor*100 + patch). */
 int pkv_version(void);
@@ -257,6 +258,25 @@ int pkv_paged_attn_decode_append_fp8(void* out, const void* q, const void* k_new
                                      int num_q_heads, int num_kv_heads, int head_dim,
                                      int block_size, float scale, void* workspace,
                                      size_t workspace_bytes, pkv_stream_t stream);
+
+/* ---- speculative verification ------------------------------------------------------------
+ * [RING] deferred speculative decoding: draft token x is accepted with probability
+ * min(1, P_target(x) / P_draft(x)); the first rejection ends the accepted run, whose rejected
+ * drafts the caller rolls back (pkv_ring_* take logical_len - rejected). With the draws given,
+ * draft k of sequence b is accepted iff u_accept[b][k] * P_draft(x) < P_target(x), P the
+ * softmax of the logits. n_accept[b] = the accepted run's length; next_token[b] = a draw
+ * (inverse CDF: the first v whose running weight exceeds u_sample[b] x the total) from the
+ * normalised residual max(0, P_target - P_draft) at the first rejected position, or from
+ * P_target at position K when all K drafts are accepted.
+ * target_logits float [num_seqs][num_drafts + 1][vocab], draft_logits float
+ * [num_seqs][num_drafts][vocab], drafts int32 [num_seqs][num_drafts], u_accept float
+ * [num_seqs][num_drafts], u_sample float [num_seqs], outputs int32 [num_seqs]; all device
+ * memory. The softmax sums are fp32 block reductions: a decision on a tie within their
+ * rounding may differ from an exact one. A draft id outside [0, vocab) counts as rejected and
+ * sets PKV_DEVERR_TOKEN. */
+int pkv_spec_verify(const float* target_logits, const float* draft_logits, const int32_t* drafts,
+                    const float* u_accept, const float* u_sample, int num_seqs, int num_drafts,
+                    int vocab, int32_t* n_accept, int32_t* next_token, pkv_stream_t stream);
 
 /* ---- host block pool ------------------------------------------------------------------------
  * The host side of paging ([OLLAMA] §三 KV Cache内存管理的工程实现, and its copy-on-write

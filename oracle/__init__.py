@@ -72,6 +72,7 @@ def _load():
             lib.pkv_orc_f64_to_e4m3.restype = ctypes.c_uint8
             lib.pkv_orc_f64_to_e4m3.argtypes = [f64]
             lib.pkv_orc_kv_append_fp8.argtypes = [P, P, P, i32, P, P, i32, i32, i32, P, P]
+            lib.pkv_orc_spec_verify.argtypes = [P, P, P, P, P, i32, i32, i32, P, P]
             lib.pkv_orc_paged_attention_fp8.restype = i32
             lib.pkv_orc_paged_attention_fp8.argtypes = [P, P, P, P, P, P, P, i32, P, i32, i32,
                                                         i32, i32, i32, i32, f64, i32]
@@ -253,3 +254,20 @@ def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, con
                                         _ptr(vs), _ptr(bt), bt.shape[1], _ptr(cl), B, q_len, Hq,
                                         Hkv, D, block_size, float(scale), num_threads)
     return out
+
+
+# --------------------------------------------------------------------------- speculative verify
+def spec_verify(target_logits, draft_logits, drafts, u_accept, u_sample):
+    """target [B, K+1, V], draft [B, K, V] float32 logits; drafts [B, K]; u_accept [B, K],
+    u_sample [B] in [0, 1) -> (n_accept [B], next_token [B]) int32."""
+    t = np.ascontiguousarray(target_logits, dtype=np.float32)
+    d = np.ascontiguousarray(draft_logits, dtype=np.float32)
+    x = _i32(drafts)
+    ua = np.ascontiguousarray(u_accept, dtype=np.float32)
+    us = np.ascontiguousarray(u_sample, dtype=np.float32)
+    B, K1, V = t.shape
+    n = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    _load().pkv_orc_spec_verify(_ptr(t), _ptr(d), _ptr(x), _ptr(ua), _ptr(us), B, K1 - 1, V,
+                                _ptr(n), _ptr(nxt))
+    return n, nxt

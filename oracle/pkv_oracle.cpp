@@ -442,4 +442,60 @@ int pkv_orc_paged_attention_fp8(double* out, const uint16_t* q, const uint8_t* k
   });
 }
 
+
+// ---------------------------------------------------------------------------
+// Speculative verification of K draft tokens per sequence.
+// [RING] (deferred speculative decoding paragraph): the target model accepts
+// draft token x with probability min(1, P_target(x) / P_draft(x)); the first
+// rejection ends the accepted run (the rejected drafts are rolled back).
+// Readings (the page leaves them to the standard method): the draws are
+// given, u_accept[b][k] in [0, 1) per draft and u_sample[b] per sequence;
+// draft k is accepted iff u_accept * P_draft(x) < P_target(x); after a
+// rejection at k the next token is drawn from the normalised residual
+// max(0, P_target - P_draft) at k, after K acceptances from P_target at
+// position K, by inverse CDF: the first v whose cumulative weight exceeds
+// u_sample times the total. P = softmax of the given logits, fp64 here.
+//   target_logits [B][K+1][V], draft_logits [B][K][V], drafts [B][K]
+// ---------------------------------------------------------------------------
+void pkv_orc_spec_verify(const float* target_logits, const float* draft_logits,
+                         const int32_t* drafts, const float* u_accept, const float* u_sample,
+                         int B, int K, int V, int32_t* n_accept, int32_t* next_token) {
+  auto softmax = [V](const float* x, std::vector<double>& p) {
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) m = std::max(m, static_cast<double>(x[v]));
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) { p[v] = std::exp(static_cast<double>(x[v]) - m); s += p[v]; }
+    for (int v = 0; v < V; ++v) p[v] /= s;
+  };
+  auto draw = [V](const std::vector<double>& w, double u) {
+    double total = 0.0;
+    for (int v = 0; v < V; ++v) total += w[v];
+    const double thr = u * total;
+    double c = 0.0;
+    for (int v = 0; v < V; ++v) {
+      c += w[v];
+      if (c > thr) return v;
+    }
+    return V - 1;
+  };
+  std::vector<double> pt(V), pd(V), r(V);
+  for (int b = 0; b < B; ++b) {
+    int k = 0;
+    for (; k < K; ++k) {
+      softmax(target_logits + (static_cast<int64_t>(b) * (K + 1) + k) * V, pt);
+      softmax(draft_logits + (static_cast<int64_t>(b) * K + k) * V, pd);
+      const int x = drafts[b * K + k];
+      if (static_cast<double>(u_accept[b * K + k]) * pd[x] < pt[x]) continue;
+      for (int v = 0; v < V; ++v) r[v] = std::max(0.0, pt[v] - pd[v]);
+      next_token[b] = draw(r, u_sample[b]);
+      break;
+    }
+    n_accept[b] = k;
+    if (k == K) {
+      softmax(target_logits + (static_cast<int64_t>(b) * (K + 1) + K) * V, pt);
+      next_token[b] = draw(pt, u_sample[b]);
+    }
+  }
+}
+
 }  // extern "C"

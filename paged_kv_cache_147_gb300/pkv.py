@@ -28,12 +28,13 @@ SYMBOLS = (
     "pkv_kv_append_fp8", "pkv_paged_attn_decode_fp8", "pkv_paged_attn_decode_append_fp8",
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocate", "pkv_pool_warm",
     "pkv_pool_release", "pkv_pool_fork", "pkv_pool_append", "pkv_pool_stats",
-    "pkv_pool_refcount",
+    "pkv_pool_refcount", "pkv_spec_verify",
 )
 
 OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
 DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_SEQ, DEVERR_POSITION = \
     1, 2, 4, 8, 16, 32
+DEVERR_TOKEN = 64
 
 
 class PkvError(RuntimeError):
@@ -108,6 +109,7 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
         "pkv_pool_append": (i32, [P, P, P, i32, i32, i32, P, P, P, i32, P]),
         "pkv_pool_stats": (i32, [P, P, P, P, P, P]),
         "pkv_pool_refcount": (i32, [P, i32]),
+        "pkv_spec_verify": (i32, [P, P, P, P, P, i32, i32, i32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name, None)    # an older build may lack newer entry points
@@ -316,6 +318,22 @@ def check_slots(slots, num_blocks, block_size) -> int | None:
         return bad.value
     _check("pkv_check_slots", st)
     return None
+
+
+# ------------------------------------------------------------------------------ speculative verify
+def spec_verify(target_logits, draft_logits, drafts, u_accept, u_sample, n_accept=None,
+                next_token=None, stream=None):
+    """target [B, K+1, V], draft [B, K, V] float32; drafts int32 [B, K]; u_accept [B, K],
+    u_sample [B] float32 -> (n_accept, next_token) int32 [B] (device tensors)."""
+    B, K1, V = target_logits.shape
+    if n_accept is None:
+        n_accept = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    _check("pkv_spec_verify", load().pkv_spec_verify(
+        _p(target_logits), _p(draft_logits), _p(drafts), _p(u_accept), _p(u_sample), B, K1 - 1,
+        V, _p(n_accept), _p(next_token), _stream(stream)))
+    return n_accept, next_token
 
 
 # ------------------------------------------------------------------------------ host block pool

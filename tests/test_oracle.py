@@ -548,3 +548,60 @@ def test_fp8_attention_equals_fp16_attention_on_the_dequantised_cache():
     assert np.array_equal(kf.astype(np.float64), oracle.e4m3_to_f64(kc8) * ks[None, :, None, None])
     want = oracle.paged_attention(q, kf, vf, bt, lens, bs, 1 / math.sqrt(d))
     assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------------------------ speculative verify
+def _softmax64(x):
+    x = np.asarray(x, np.float64)
+    e = np.exp(x - x.max(-1, keepdims=True))
+    return e / e.sum(-1, keepdims=True)
+
+
+def test_spec_verify_identical_models_accept_every_draft():
+    rng = np.random.default_rng(31)
+    B, K, V = 6, 4, 40
+    t = rng.standard_normal((B, K + 1, V)).astype(np.float32)
+    d = t[:, :K].copy()
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    ua = rng.random((B, K)).astype(np.float32)
+    us = rng.random(B).astype(np.float32)
+    n, nxt = oracle.spec_verify(t, d, x, ua, us)
+    assert np.all(n == K)
+    # the bonus token: inverse CDF of the target's last position (first v with cdf > u)
+    cdf = np.cumsum(_softmax64(t[:, K]), axis=-1)
+    want = [int(np.searchsorted(cdf[b], float(us[b]) * cdf[b, -1], side="right"))
+            for b in range(B)]
+    assert list(nxt) == want
+
+
+def test_spec_verify_two_token_closed_form():
+    # draft P = (1/2, 1/2), target P = (1/4, 3/4): token 0 survives iff u < 1/2 and a rejection
+    # always yields token 1 (the only positive residual); token 1 (ratio 3/2) always survives
+    t = np.array([[[0.0, math.log(3.0)], [0.0, 0.0]]], np.float32)
+    d = np.array([[[0.0, 0.0]]], np.float32)
+    for u, acc in ((0.49, 1), (0.51, 0)):
+        n, nxt = oracle.spec_verify(t, d, np.array([[0]]), np.array([[u]]), np.array([0.3]))
+        assert n[0] == acc
+        if not acc:
+            assert nxt[0] == 1
+    n, _ = oracle.spec_verify(t, d, np.array([[1]]), np.array([[0.999]]), np.array([0.3]))
+    assert n[0] == 1
+
+
+def test_spec_verify_first_token_follows_the_target_distribution():
+    # speculative sampling's defining property: the first emitted token (the draft if accepted,
+    # else the residual draw) is distributed as the target, whatever the draft distribution
+    rng = np.random.default_rng(32)
+    V, N = 6, 40000
+    t = rng.standard_normal((1, 2, V)).astype(np.float32)
+    d = (rng.standard_normal((1, 1, V)) * 1.5).astype(np.float32)
+    pd = _softmax64(d[0, 0])
+    x = rng.choice(V, size=N, p=pd).astype(np.int32)[:, None]
+    ua = rng.random((N, 1)).astype(np.float32)
+    us = rng.random(N).astype(np.float32)
+    tt = np.repeat(t, N, axis=0)
+    dd = np.repeat(d, N, axis=0)
+    n, nxt = oracle.spec_verify(tt, dd, x, ua, us)
+    first = np.where(n >= 1, x[:, 0], nxt)
+    freq = np.bincount(first, minlength=V) / N
+    assert np.max(np.abs(freq - _softmax64(t[0, 0]))) < 0.012
