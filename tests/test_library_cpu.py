@@ -87,3 +87,26 @@ def test_workload_structure(name):
     if name == "ring":
         assert w.block_tables.shape[1] * w.block_size == w.sink + w.window
         assert (w.ring_len0 >= 2000).all() and (w.ring_len0 <= 100000).all()
+
+
+def test_new_entry_points_reject_bad_arguments_before_any_launch(lib):
+    # argument checks run on the host before any CUDA call, so they are testable here
+    n, t = ctypes.c_int(0), ctypes.c_int(0)
+    assert lib.pkv_spec_verify(None, None, None, None, None, -1, 4, 100, None, None,
+                               None) == pkv.EINVAL
+    assert lib.pkv_spec_verify(None, None, None, None, None, 4, 4, 0, None, None,
+                               None) == pkv.EINVAL
+    assert lib.pkv_spec_verify(None, None, None, None, None, 0, 4, 100, None, None,
+                               None) == pkv.OK                      # nothing to do
+    assert lib.pkv_kv_append_fp8(None, None, None, 4, None, None, 8, 2, 128, 16, None, None,
+                                 None) == pkv.EINVAL                # no pointers, no scales
+    assert lib.pkv_kv_append_fp8(None, None, None, 1, None, None, 8, 2, 128, 24, None, None,
+                                 None) == pkv.EINVAL                # block size 24
+    assert lib.pkv_paged_attn_decode_fp8(None, None, None, None, None, None, 8, None, 4, None,
+                                         2, 1, 12, 2, 128, 16, 0.1, None, 0,
+                                         None) == pkv.EINVAL        # scales missing
+    assert lib.pkv_paged_attn_decode_append_fp8(None, None, None, None, None, None, None, None,
+                                                8, None, 4, None, 2, 1, 12, 2, 128, 16, 0.1,
+                                                None, 0, None) == pkv.EINVAL
+    assert lib.pkv_pool_create(0, 16, 64, None) == pkv.EINVAL
+    assert lib.pkv_pool_stats(None, None, None, None, None, None) == pkv.EINVAL
