@@ -8,7 +8,10 @@
  *   - copy-on-write block copy;
  *   - paged decode attention: each sequence's few newest query tokens attend over all of its
  *     cached K/V, read indirectly through its block table, with GQA head groups;
- *   - sink + ring decode attention with RoPE applied at read time.
+ *   - sink + ring decode attention with RoPE applied at read time;
+ * and around it: an FP8 (E4M3) form of the cache with its append and decode, verification of
+ * speculative drafts (accept/reject, next token), and a host block pool that hands out the
+ * block tables (prefix sharing, reference counts, copy-on-write pairs).
  *
  * Sources (page title, section):
  *   [EDGE]   "端侧 SLM 显存保活术：在 4GB 内存板卡上实现轻量 PagedAttention 与 KV 缓存分块"
@@ -20,7 +23,8 @@
  * Conventions shared by every entry point
  *   - Pointers marked (device) are CUDA device pointers; (host) are host pointers. The caller
  *     owns every buffer. Nothing here allocates device memory or synchronises the stream,
- *     except pkv_device_error(), which reads a status word back.
+ *     except pkv_device_error(), which reads a status word back (the host block pool
+ *     allocates its own host bookkeeping).
  *   - fp16 tensors are IEEE binary16 ("half"), passed as void*.
  *   - One layer's KV pool: k_cache and v_cache, each [num_blocks][num_kv_heads][block_size]
  *     [head_dim] contiguous, 16-byte aligned. Several layers are addressed by the caller
