@@ -13,7 +13,7 @@
 
 namespace {
 
-constexpr int kSpecThreads = 256;
+constexpr int kSpecThreads = 1024;
 
 __device__ __forceinline__ float block_max(float v, float* sh) {
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
