@@ -200,3 +200,29 @@ def test_library_pool_rejects_bad_arguments_without_change():
     with pytest.raises(pkv.PkvError):
         lib.release(t)                                    # no longer held
     assert lib.stats()["free"] == 8
+
+
+def test_model_reuse_equals_longest_common_block_prefix():
+    # with nothing released, a new prompt reuses exactly as many leading full blocks as the
+    # longest full-block prefix it shares with any earlier prompt (brute force over pairs)
+    rng = np.random.default_rng(5)
+    bs = 3
+    p = blocks.BlockPool(2000, bs)
+    lib = pkv.BlockPool(2000, bs)
+    stems = [list(rng.integers(0, 3, 12)) for _ in range(4)]
+    seen = []
+    for _ in range(120):
+        s = stems[rng.integers(len(stems))]
+        cut = int(rng.integers(0, 13))
+        toks = s[:cut] + list(rng.integers(0, 3, rng.integers(0, 7)))
+        want = 0
+        for prev in seen:
+            k = 0
+            while (k + 1) * bs <= min(len(prev), len(toks)) and \
+                    prev[k * bs:(k + 1) * bs] == toks[k * bs:(k + 1) * bs]:
+                k += 1
+            want = max(want, k)
+        _, r = p.allocate(toks)
+        _, rl = lib.allocate(toks)
+        assert r == want == rl
+        seen.append(toks)
