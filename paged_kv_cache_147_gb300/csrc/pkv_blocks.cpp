@@ -16,6 +16,7 @@
 #include <deque>
 #include <mutex>
 #include <new>
+#include <set>
 #include <unordered_map>
 #include <utility>
 #include <vector>
@@ -32,6 +33,8 @@ struct pkv_block_pool {
   std::vector<std::vector<int32_t>> toks;
   std::deque<int> free_list;
   std::unordered_map<uint64_t, std::vector<int>> index;   // key -> blocks, registration order
+  std::set<std::pair<int64_t, int>> warm;                // (allocation stamp, block) of the
+                                                         // indexed blocks nobody holds
   int64_t clock = 0;
   std::mutex mu;
 };
@@ -51,6 +54,7 @@ uint64_t fnv1a(const int32_t* t, int n, uint64_t h) {
 
 void unindex(pkv_block_pool* p, int b) {
   if (!p->indexed[b]) return;
+  if (p->ref[b] == 0) p->warm.erase({p->stamp[b], b});
   auto it = p->index.find(p->key[b]);
   if (it != p->index.end()) {
     auto& v = it->second;
@@ -70,6 +74,16 @@ void index_block(pkv_block_pool* p, int b, int parent, uint64_t chain, const int
   p->index[p->key[b]].push_back(b);
 }
 
+// Reference changes keep the warm set: an indexed block enters it at reference 0 and leaves it
+// when it is held again (or unindexed).
+void inc_ref(pkv_block_pool* p, int b) {
+  if (p->ref[b]++ == 0 && p->indexed[b]) p->warm.erase({p->stamp[b], b});
+}
+
+void dec_ref(pkv_block_pool* p, int b) {
+  if (--p->ref[b] == 0 && p->indexed[b]) p->warm.insert({p->stamp[b], b});
+}
+
 int match(pkv_block_pool* p, int parent, uint64_t chain, const int32_t* t) {
   auto it = p->index.find(chain & p->mask);
   if (it == p->index.end()) return -1;
@@ -82,15 +96,12 @@ int match(pkv_block_pool* p, int parent, uint64_t chain, const int32_t* t) {
 // blocks (oldest allocation first) if it is short. All or nothing.
 bool take(pkv_block_pool* p, int n, std::vector<int>& out) {
   if (static_cast<int>(p->free_list.size()) < n) {
-    std::vector<std::pair<int64_t, int>> warm;
-    for (int b = 0; b < p->nb; ++b)
-      if (p->ref[b] == 0 && p->indexed[b]) warm.emplace_back(p->stamp[b], b);
     const int need = n - static_cast<int>(p->free_list.size());
-    if (static_cast<int>(warm.size()) < need) return false;
-    std::sort(warm.begin(), warm.end());
+    if (static_cast<int>(p->warm.size()) < need) return false;
     for (int i = 0; i < need; ++i) {
-      unindex(p, warm[i].second);
-      p->free_list.push_back(warm[i].second);
+      const int b = p->warm.begin()->second;      // oldest allocation first
+      unindex(p, b);
+      p->free_list.push_back(b);
     }
   }
   for (int i = 0; i < n; ++i) {
@@ -129,10 +140,10 @@ int allocate_locked(pkv_block_pool* p, const int32_t* tokens, int n_tokens, int 
   const int n_reused = static_cast<int>(got.size());
   const int need = (max_tokens - pos + bs - 1) / bs;
   if (n_reused + need > table_cap) return PKV_EINVAL;
-  for (int b : got) ++p->ref[b];
+  for (int b : got) inc_ref(p, b);
   std::vector<int> fresh;
   if (!take(p, need, fresh)) {
-    for (int b : got) --p->ref[b];
+    for (int b : got) dec_ref(p, b);
     return PKV_ENOSPC;
   }
   for (int b : fresh) {
@@ -196,7 +207,7 @@ int pkv_pool_warm(pkv_block_pool* pool, const int32_t* tokens, int n_tokens) {
   const int st = allocate_locked(pool, tokens, full, full, table.data(),
                                  static_cast<int>(table.size()), &n, nullptr);
   if (st != PKV_OK) return st;
-  for (int i = 0; i < n; ++i) --pool->ref[table[i]];
+  for (int i = 0; i < n; ++i) dec_ref(pool, table[i]);
   return PKV_OK;
 }
 
@@ -206,7 +217,8 @@ int pkv_pool_release(pkv_block_pool* pool, const int32_t* table, int n_blocks) {
   if (!valid_table(pool, table, n_blocks)) return PKV_EINVAL;
   for (int i = 0; i < n_blocks; ++i) {
     const int b = table[i];
-    if (--pool->ref[b] == 0) {
+    dec_ref(pool, b);
+    if (pool->ref[b] == 0) {
       unindex(pool, b);
       pool->free_list.push_back(b);
     }
@@ -218,7 +230,7 @@ int pkv_pool_fork(pkv_block_pool* pool, const int32_t* table, int n_blocks) {
   if (!pool) return PKV_EINVAL;
   std::lock_guard<std::mutex> lock(pool->mu);
   if (!valid_table(pool, table, n_blocks)) return PKV_EINVAL;
-  for (int i = 0; i < n_blocks; ++i) ++pool->ref[table[i]];
+  for (int i = 0; i < n_blocks; ++i) inc_ref(pool, table[i]);
   return PKV_OK;
 }
 
@@ -250,7 +262,7 @@ int pkv_pool_append(pkv_block_pool* pool, int32_t* table, int* n_blocks, int tab
     if (j < nb0 && pool->ref[table[j]] > 1) {
       const int d = fresh[used++];
       pool->ref[d] = 1;
-      --pool->ref[table[j]];
+      dec_ref(pool, table[j]);
       copy_src[*n_copies] = table[j];
       copy_dst[*n_copies] = d;
       ++*n_copies;
@@ -281,12 +293,12 @@ int pkv_pool_stats(pkv_block_pool* pool, int* total, int* used, int* shared, int
                    int* warm) {
   if (!pool) return PKV_EINVAL;
   std::lock_guard<std::mutex> lock(pool->mu);
-  int u = 0, s = 0, w = 0;
+  int u = 0, s = 0;
   for (int b = 0; b < pool->nb; ++b) {
     u += pool->ref[b] > 0;
     s += pool->ref[b] > 1;
-    w += pool->ref[b] == 0 && pool->indexed[b];
   }
+  const int w = static_cast<int>(pool->warm.size());
   if (total) *total = pool->nb;
   if (used) *used = u;
   if (shared) *shared = s;
