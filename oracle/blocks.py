@@ -18,13 +18,18 @@ paragraph), with the readings the page leaves open made explicit:
   blocks while they match (reference +1), stop at the first miss; then take
   ceil((max_tokens - reused tokens) / block_size) new blocks (reference 1) and index the new
   full prompt blocks.
-* release(table): reference -1 per block; a block that reaches 0 leaves the index and goes to
-  the back of the free list.
+* release(table): reference -1 per block; a block that reaches 0 goes to the back of the free
+  list and leaves the index.
+* Leaving the index: a block's indexed descendants (children matched under it, their children,
+  ...) leave the index with it, because its id may then be handed out for other tokens and a
+  child's parent check would no longer prove its prefix. Descendants no sequence holds go to
+  the back of the free list, a block before its own descendants, children in registration
+  order.
 * warm(tokens): index a prompt's full blocks without a sequence holding them (reference 0,
   off the free list): the page's pre-warmed system prompt.
-* eviction: when the free list is short, indexed blocks no sequence holds (warm ones) are
-  reclaimed, oldest allocation first (the page's LRU proxy); blocks a sequence holds are never
-  taken. Not enough: out of memory (no change).
+* eviction: while the free list is short, the oldest (by allocation) indexed block no sequence
+  holds (a warm one) is reclaimed (the page's LRU proxy); blocks a sequence holds are never
+  taken. Fewer free and warm blocks than asked for: out of memory (no change).
 * fork(table): a child sharing every block of its parent (reference +1 each).
 * append(table, length, n_new, new_tokens): make room for positions [length, length + n_new):
   a position past the table takes a new block; a position in a block other sequences also
@@ -60,21 +65,21 @@ class BlockPool:
         self.chain = [0] * num_blocks           # FNV state after the block's last token
         self.toks = [None] * num_blocks         # token ids of an indexed block
         self.parent = [-1] * num_blocks         # block matched before it (-1: first block)
+        self.kids = [[] for _ in range(num_blocks)]   # indexed children, registration order
         self.stamp = [0] * num_blocks           # allocation order
         self.clock = 0
         self.index = {}                         # key -> [blocks], in registration order
 
     # ---------------------------------------------------------------- internals
     def _take(self, n):
-        if len(self.free) < n:
-            warm = sorted((self.stamp[b], b) for b in range(self.nb)
-                          if self.ref[b] == 0 and self.key[b] is not None)
-            need = n - len(self.free)
-            if len(warm) < need:
-                raise OutOfBlocks()
-            for _, b in warm[:need]:
-                self._unindex(b)
-                self.free.append(b)
+        warm = [b for b in range(self.nb) if self.ref[b] == 0 and self.key[b] is not None]
+        if len(self.free) + len(warm) < n:
+            raise OutOfBlocks()
+        while len(self.free) < n:
+            oldest = min((self.stamp[b], b) for b in range(self.nb)
+                         if self.ref[b] == 0 and self.key[b] is not None)[1]
+            self.free.append(oldest)
+            self._unindex(oldest)
         out = []
         for _ in range(n):
             b = self.free.pop(0)
@@ -91,13 +96,25 @@ class BlockPool:
         lst.remove(b)
         if not lst:
             del self.index[k]
+        if self.parent[b] >= 0 and b in self.kids[self.parent[b]]:
+            self.kids[self.parent[b]].remove(b)
         self.key[b] = None
         self.toks[b] = None
+        kids, self.kids[b] = self.kids[b], []
+        for c in kids:
+            if self.key[c] is None:
+                continue
+            self.parent[c] = -1
+            if self.ref[c] == 0:
+                self.free.append(c)
+            self._unindex(c)
 
     def _index_block(self, b, parent, chain, toks):
         k = chain & self.hash_mask
         self.key[b], self.chain[b], self.toks[b], self.parent[b] = k, chain, list(toks), parent
         self.index.setdefault(k, []).append(b)
+        if parent >= 0:
+            self.kids[parent].append(b)
 
     def _match(self, parent, chain, toks):
         for b in self.index.get(chain & self.hash_mask, []):
@@ -143,15 +160,15 @@ class BlockPool:
         table, reused = self.allocate(list(tokens)[:full])
         for b in table:
             self.ref[b] -= 1
-        return table
+        return table, reused
 
     def release(self, table):
         for b in table:
             self.ref[b] -= 1
             assert self.ref[b] >= 0
             if self.ref[b] == 0:
-                self._unindex(b)
                 self.free.append(b)
+                self._unindex(b)
 
     def fork(self, table):
         for b in table:

@@ -7,10 +7,13 @@
 // Readings of the page (it leaves them open): a block's index key is the FNV-1a state after
 // its last token continued from its parent block's (a chain over the whole prefix); only full
 // blocks are indexed; a candidate is accepted only if its token ids and its parent block match
-// (the token-level verification the page asks for against collisions); releasing the last
-// reference frees a block and removes it from the index; warm() indexes a prompt's blocks with
-// no reference (the page's pre-warmed system prompt); when the free list is short, indexed
-// unreferenced blocks are reclaimed oldest allocation first, and referenced blocks never are.
+// (the token-level verification the page asks for against collisions); a block that leaves the
+// index takes its indexed descendants with it (their parent id may be reused for other tokens,
+// so the parent check would no longer prove the prefix), and those nobody holds are freed;
+// releasing the last reference frees a block and removes it from the index; warm() indexes a
+// prompt's blocks with no reference (the page's pre-warmed system prompt); when the free list
+// is short, indexed unreferenced blocks are reclaimed oldest allocation first, and referenced
+// blocks never are.
 #include <algorithm>
 #include <cstdint>
 #include <deque>
@@ -31,6 +34,7 @@ struct pkv_block_pool {
   std::vector<uint64_t> key, chain;
   std::vector<int64_t> stamp;
   std::vector<std::vector<int32_t>> toks;
+  std::vector<std::vector<int>> kids;                    // indexed children, registration order
   std::deque<int> free_list;
   std::unordered_map<uint64_t, std::vector<int>> index;   // key -> blocks, registration order
   std::set<std::pair<int64_t, int>> warm;                // (allocation stamp, block) of the
@@ -52,6 +56,10 @@ uint64_t fnv1a(const int32_t* t, int n, uint64_t h) {
   return h;
 }
 
+// Removes b from the index. Its indexed descendants leave the index with it: once b's id can
+// be handed out for other tokens, a child's (parent id, tokens) check no longer proves that the
+// child follows the same prefix. A descendant nobody holds goes to the back of the free list
+// (pre-order: a block before its own descendants, children in registration order).
 void unindex(pkv_block_pool* p, int b) {
   if (!p->indexed[b]) return;
   if (p->ref[b] == 0) p->warm.erase({p->stamp[b], b});
@@ -61,8 +69,22 @@ void unindex(pkv_block_pool* p, int b) {
     v.erase(std::find(v.begin(), v.end(), b));
     if (v.empty()) p->index.erase(it);
   }
+  const int par = p->parent[b];
+  if (par >= 0) {
+    auto& k = p->kids[par];
+    auto kt = std::find(k.begin(), k.end(), b);
+    if (kt != k.end()) k.erase(kt);
+  }
   p->indexed[b] = 0;
   p->toks[b].clear();
+  std::vector<int> kids;
+  kids.swap(p->kids[b]);
+  for (int c : kids) {
+    if (!p->indexed[c]) continue;
+    p->parent[c] = -1;                    // b's list is already detached
+    if (p->ref[c] == 0) p->free_list.push_back(c);
+    unindex(p, c);
+  }
 }
 
 void index_block(pkv_block_pool* p, int b, int parent, uint64_t chain, const int32_t* t) {
@@ -72,6 +94,7 @@ void index_block(pkv_block_pool* p, int b, int parent, uint64_t chain, const int
   p->parent[b] = parent;
   p->toks[b].assign(t, t + p->bs);
   p->index[p->key[b]].push_back(b);
+  if (parent >= 0) p->kids[parent].push_back(b);
 }
 
 // Reference changes keep the warm set: an indexed block enters it at reference 0 and leaves it
@@ -95,14 +118,13 @@ int match(pkv_block_pool* p, int parent, uint64_t chain, const int32_t* t) {
 // Takes n blocks from the front of the free list, first reclaiming indexed unreferenced
 // blocks (oldest allocation first) if it is short. All or nothing.
 bool take(pkv_block_pool* p, int n, std::vector<int>& out) {
-  if (static_cast<int>(p->free_list.size()) < n) {
-    const int need = n - static_cast<int>(p->free_list.size());
-    if (static_cast<int>(p->warm.size()) < need) return false;
-    for (int i = 0; i < need; ++i) {
-      const int b = p->warm.begin()->second;      // oldest allocation first
-      unindex(p, b);
-      p->free_list.push_back(b);
-    }
+  // eviction moves warm blocks (and orphaned warm descendants) to the free list, so free +
+  // warm is what can be had
+  if (static_cast<int>(p->free_list.size() + p->warm.size()) < n) return false;
+  while (static_cast<int>(p->free_list.size()) < n) {
+    const int b = p->warm.begin()->second;        // oldest allocation first
+    p->free_list.push_back(b);
+    unindex(p, b);
   }
   for (int i = 0; i < n; ++i) {
     const int b = p->free_list.front();
@@ -182,6 +204,7 @@ int pkv_pool_create(int num_blocks, int block_size, int hash_bits, pkv_block_poo
   p->chain.assign(num_blocks, 0);
   p->stamp.assign(num_blocks, 0);
   p->toks.assign(num_blocks, {});
+  p->kids.assign(num_blocks, {});
   for (int b = 0; b < num_blocks; ++b) p->free_list.push_back(b);
   *out = p;
   return PKV_OK;
@@ -219,8 +242,8 @@ int pkv_pool_release(pkv_block_pool* pool, const int32_t* table, int n_blocks) {
     const int b = table[i];
     dec_ref(pool, b);
     if (pool->ref[b] == 0) {
-      unindex(pool, b);
       pool->free_list.push_back(b);
+      unindex(pool, b);
     }
   }
   return PKV_OK;

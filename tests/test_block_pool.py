@@ -110,11 +110,52 @@ def test_model_warm_blocks_are_reused_then_reclaimed_oldest_first():
         p.allocate([8, 8])
 
 
+def test_model_evicting_a_parent_drops_its_children_from_the_index():
+    # Two warm blocks [1,2] -> [3,4]; a new prompt evicts the parent [1,2] and its id is
+    # re-indexed for [5,6]. The child [3,4] followed [1,2], not [5,6], so a prompt [5,6,3,4]
+    # may reuse only its first block. (With a 1-bit key every block collides: only the
+    # parent and token checks stand between the prompt and the stale child.)
+    for make in (lambda: blocks.BlockPool(2, 2, hash_bits=1),
+                 lambda: pkv.BlockPool(2, 2, 1)):
+        p = make()
+        p.warm([1, 2, 3, 4])
+        t1, r1 = p.allocate([5, 6])
+        assert r1 == 0 and list(t1) == [0]
+        t2, r2 = p.allocate([5, 6, 3, 4])
+        assert r2 == 1 and list(t2) == [0, 1]
+        if hasattr(p, "close"):
+            p.close()
+
+
+class _Shadow:
+    """What each physical block really holds: the token prefix, from position 0, that was
+    current when its last row was written (copies carry it over). A reused block is correct
+    only if its prefix equals the new prompt's."""
+
+    def __init__(self, nb, bs):
+        self.bs = bs
+        self.held = [()] * nb
+
+    def allocated(self, table, reused, toks):
+        for j in range(reused):
+            assert self.held[table[j]] == tuple(toks[:(j + 1) * self.bs]), (j, table[j])
+        for j in range(reused, len(table)):
+            end = min((j + 1) * self.bs, len(toks))
+            self.held[table[j]] = tuple(toks[:end]) if j * self.bs < len(toks) else ()
+
+    def appended(self, table, copies, length, n, toks):
+        for src, dst in copies:
+            self.held[dst] = self.held[src]
+        for j in range(length // self.bs, (length + n - 1) // self.bs + 1):
+            self.held[table[j]] = tuple(toks[:min((j + 1) * self.bs, length + n)])
+
+
 # ------------------------------------------------------------------------------ library == model
 def _random_ops(seed, nb=48, bs=4, steps=400, hash_bits=64):
     rng = np.random.default_rng(seed)
     lib = pkv.BlockPool(nb, bs, hash_bits)
     ref = blocks.BlockPool(nb, bs, hash_bits)
+    shadow = _Shadow(nb, bs)
     prompts = [list(rng.integers(0, 50, rng.integers(0, 14))) for _ in range(5)]
     live = {}     # name -> (table, length, tokens)
     nid = 0
@@ -133,6 +174,7 @@ def _random_ops(seed, nb=48, bs=4, steps=400, hash_bits=64):
                 continue
             tl, rl = lib.allocate(toks, mt)
             assert list(tl) == tr and rl == rr, step
+            shadow.allocated(tr, rr, toks)
             live[nid] = (tr, len(toks), toks)
             nid += 1
         elif op == "append":
@@ -148,6 +190,7 @@ def _random_ops(seed, nb=48, bs=4, steps=400, hash_bits=64):
                 continue
             tl, cl = lib.append(np.asarray(t, np.int32), L, n, all_tokens=toks2)
             assert list(tl) == tr and [tuple(x) for x in cl.tolist()] == cr, step
+            shadow.appended(tr, cr, L, n, toks2)
             live[k] = (tr, L + n, toks2)
         elif op == "fork":
             k = list(live)[rng.integers(len(live))]
@@ -164,12 +207,13 @@ def _random_ops(seed, nb=48, bs=4, steps=400, hash_bits=64):
         else:
             toks = prompts[rng.integers(len(prompts))]
             try:
-                ref.warm(toks)
+                tw, rw = ref.warm(toks)
             except blocks.OutOfBlocks:
                 with pytest.raises(pkv.PkvError):
                     lib.warm(toks)
                 continue
             lib.warm(toks)
+            shadow.allocated(tw, rw, toks[:(len(toks) // bs) * bs])
         assert lib.stats() == ref.stats(), (step, op)
         assert [lib.refcount(b) for b in range(nb)] == ref.ref, (step, op)
     _check_invariants(ref, {k: v[0] for k, v in live.items()})
@@ -183,6 +227,13 @@ def test_library_pool_equals_model(seed):
 
 def test_library_pool_equals_model_under_collisions_and_pressure():
     _random_ops(7, nb=20, bs=2, steps=600, hash_bits=3)
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_reused_blocks_hold_the_prompt_prefix_under_eviction(seed):
+    # tiny pools, one-bit keys and few distinct tokens: parents are evicted and their ids
+    # reused all the time; every reused block must still hold exactly the prompt's prefix
+    _random_ops(seed, nb=10, bs=2, steps=800, hash_bits=1)
 
 
 def test_library_pool_rejects_bad_arguments_without_change():
