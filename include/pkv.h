@@ -128,6 +128,14 @@ int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int3
  * PKV_DEVERR_TIMEOUT, re-initialise it. */
 size_t pkv_decode_workspace_bytes(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
                                   int head_dim);
+
+/* Turns the launch overlap of the fused-append calls (pkv_paged_attn_decode_append and its FP8
+ * form) on (enable != 0, the default) or off, for every call made afterwards in this process,
+ * including calls captured into a CUDA graph afterwards. With it off a fused call starts only
+ * after the kernel before it has completed, so it may follow a kernel that writes its pools,
+ * block tables or context lengths. Returns the previous setting (0 or 1). Not part of the
+ * pages' design: a scheduling control of this implementation. */
+int pkv_set_early_start(int enable);
 int pkv_workspace_init(void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /* Paged decode attention ([VLLM] PagedAttention kernel paragraph: K/V read indirectly through
@@ -156,12 +164,15 @@ int pkv_paged_attn_decode(void* out, const void* q, const void* k_cache, const v
  * and used both for the pool and for this step's attention. k_new, v_new (device): fp16
  * [num_seqs * q_len][num_kv_heads][head_dim]; other arguments as for pkv_paged_attn_decode. The
  * slots written must not be shared with another sequence (copy-on-write first).
- * Launch overlap: this call is launched with programmatic dependent launch, so it may start
- * while the kernel before it on the stream is still finishing. Before that kernel completes it
- * reads only the K/V pools, block_tables and context_lens; q, k_new, v_new, out and the workspace
- * are touched after. Those three inputs must therefore not be written by the immediately
- * preceding kernel (in particular not by a preceding pkv_paged_attn_decode_append on the same
- * pools). The library's other kernels never let the next kernel start early. */
+ * Launch overlap: by default this call is launched with programmatic dependent launch, so it
+ * may start while the kernel before it on the stream is still finishing. Before that kernel
+ * completes it reads only the K/V pools, block_tables and context_lens; q, k_new, v_new, out and
+ * the workspace are touched after. Those three inputs must therefore not be written by the
+ * immediately preceding kernel: not by a preceding pkv_paged_attn_decode_append on the same
+ * pools, not by pkv_copy_blocks, and not by the caller's own kernel (say, one that advances
+ * context_lens on the device). A copy (cudaMemcpyAsync) or any other kernel in between is
+ * enough; otherwise turn the overlap off with pkv_set_early_start(0). The library's other
+ * kernels never let the next kernel start early. */
 int pkv_paged_attn_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
                                  void* k_cache, void* v_cache, int num_blocks,
                                  const int32_t* block_tables, int max_blocks_per_seq,
@@ -178,9 +189,13 @@ int pkv_paged_attn_decode_append(void* out, const void* q, const void* k_new, co
  * memory budget, or at a point where entering an allocator is not allowed. The pages have no
  * counterpart of this entry point; it is an integration convenience.
  *   - The array is 8 MiB, held by every GPU that loads the library until the process exits.
- *     A call whose scratch would not fit (2 * SMs * 4 partial records of
- *     (num_q_heads / num_kv_heads) * q_len rows of 528 bytes, plus 4 bytes per sequence and kv
- *     head: for example up to 8 rows on a 152-SM GPU) returns PKV_ENOSPC and launches nothing.
+ *     With R = (num_q_heads / num_kv_heads) * q_len rows per unit and S the device's SM count,
+ *     a call fits if  up(4 * num_seqs * num_kv_heads) + up(8 * S * R * 16) + up(8 * S * R * 512)
+ *     <= 8 MiB, where up() rounds up to a multiple of 256 (arrival counters, then the (m, l)
+ *     and o[128] records of 2 partials for each of up to 4 CTAs per SM). On a 152-SM GPU that
+ *     is R <= 13 (for num_seqs * num_kv_heads <= 10496). A call that does not fit returns
+ *     PKV_ENOSPC and launches nothing. Shapes pkv_paged_attn_decode rejects return PKV_EINVAL,
+ *     also for num_seqs == 0; a batch of 0 sequences with valid shapes returns PKV_OK.
  *   - It allocates nothing: no cudaMalloc, no cudaFree. Each call clears the arrival counters
  *     with one cudaMemsetAsync on `stream`, then launches the decode kernel.
  *   - The first call on a device resolves the array's device address (cudaGetSymbolAddress)

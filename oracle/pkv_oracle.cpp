@@ -17,8 +17,8 @@
 //   [VLLM]   "大模型推理内存优化：从 KV Cache 分页到连续批处理的工程实践"
 //             (pwwt.cn/news/3010209)
 //
-// Conventions fixed here (the pages are silent on them; each is one of the
-// readings listed in the design notes):
+// Conventions fixed here (the pages are silent on them, so each is a reading of
+// them, chosen as the plainest one the rest of the pages support):
 //   * KV pool of one layer: [num_blocks][num_kv_heads][block_size][head_dim],
 //     fp16 stored as raw uint16 bit patterns, K and V in separate pools.
 //   * GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).

@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -1469,6 +1470,10 @@ constexpr int kNCWFp8 = PKV_FP8_WARPS, kNSTFp8 = PKV_FP8_STAGES;
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, DecodeArgs);
 
+// Whether the fused-append calls may start while the kernel before them finishes
+// (programmatic dependent launch); process-wide, read at each launch.
+std::atomic<int> g_early_start{1};
+
 struct Variant {
   const void* fn;
   int mt;
@@ -1665,7 +1670,7 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = append ? 1 : 0;
+  cfg.numAttrs = (append && g_early_start.load(std::memory_order_relaxed)) ? 1 : 0;
   return cuda_status(cudaLaunchKernelExC(&cfg, v.fn, params));
 }
 
@@ -1713,6 +1718,10 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int q_len, int num_q_heads, int 
     return 0;
   const int R = num_q_heads / num_kv_heads * q_len;
   return ws_layout(std::max(num_seqs, 1), num_kv_heads, R).total;
+}
+
+int pkv_set_early_start(int enable) {
+  return g_early_start.exchange(enable != 0 ? 1 : 0);
 }
 
 int pkv_workspace_init(void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
@@ -1795,24 +1804,26 @@ int pkv_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache,
                                   const int32_t* context_lens, int num_seqs, int q_len,
                                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                   float scale, pkv_stream_t stream) {
-  if (num_seqs > 0 && q_len >= 1 && num_q_heads >= 1 && num_kv_heads >= 1 &&
-      num_q_heads % num_kv_heads == 0 && head_dim == kD) {
-    const int R = num_q_heads / num_kv_heads * q_len;
-    if (sm_count() == 0) return cuda_status(cudaGetLastError());
-    const WsLayout ws = ws_layout(num_seqs, num_kv_heads, R);
-    if (ws.total > kFixedScratchBytes) return PKV_ENOSPC;
-    int status = PKV_OK;
-    void* scratch = fixed_scratch(&status);
-    if (!scratch) return status;
-    // the array keeps the previous call's contents; the arrival counters must start at zero
-    const cudaError_t e = cudaMemsetAsync(scratch, 0, ws.part_ml, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_status(e);
-    return pkv_paged_attn_decode(out, q, k_cache, v_cache, num_blocks, block_tables,
-                                 max_blocks_per_seq, context_lens, num_seqs, q_len, num_q_heads,
-                                 num_kv_heads, head_dim, block_size, scale, scratch,
-                                 kFixedScratchBytes, stream);
-  }
-  return num_seqs == 0 ? PKV_OK : PKV_EINVAL;
+  // the shape checks of pkv_paged_attn_decode, before anything else (an empty batch included)
+  if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 ||
+      num_q_heads % num_kv_heads != 0 || head_dim != kD || !valid_block_size(block_size) ||
+      num_blocks < 0 || max_blocks_per_seq < 0 || num_q_heads / num_kv_heads * q_len > 32)
+    return PKV_EINVAL;
+  if (num_seqs == 0) return PKV_OK;
+  if (sm_count() == 0) return PKV_EINVAL;   // no usable current device
+  const int R = num_q_heads / num_kv_heads * q_len;
+  const WsLayout ws = ws_layout(num_seqs, num_kv_heads, R);
+  if (ws.total > kFixedScratchBytes) return PKV_ENOSPC;
+  int status = PKV_OK;
+  void* scratch = fixed_scratch(&status);
+  if (!scratch) return status;
+  // the array keeps the previous call's contents; the arrival counters must start at zero
+  const cudaError_t e = cudaMemsetAsync(scratch, 0, ws.part_ml, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  return pkv_paged_attn_decode(out, q, k_cache, v_cache, num_blocks, block_tables,
+                               max_blocks_per_seq, context_lens, num_seqs, q_len, num_q_heads,
+                               num_kv_heads, head_dim, block_size, scale, scratch,
+                               kFixedScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -58,8 +58,10 @@ def test_pool_driven_prefix_batch_with_fork_and_copy_on_write():
     for b, t in enumerate(tables):
         bt[b, :len(t)] = t
     # every sequence's new slot is its own: no shared block is written
-    slots = [int(bt[b, (L - 1) // bs]) * bs + (L - 1) % bs for b, L in enumerate(lens)]
-    assert len(set(slots)) == n_seq and all(pool.refcount(s // bs) == 1 for s in slots)
+    slots = oracle.slot_mapping(np.arange(n_seq, dtype=np.int32), lens.astype(np.int64) - 1,
+                                bt, bs)
+    assert len(set(slots.tolist())) == n_seq and all(pool.refcount(int(s) // bs) == 1
+                                                     for s in slots)
 
     nb = pool.num_blocks
     k = torch.randn((nb, hkv, bs, 128), device=DEV).half()
@@ -80,7 +82,7 @@ def test_pool_driven_prefix_batch_with_fork_and_copy_on_write():
                                  _dev(lens, torch.int32), scale, ws)
     torch.cuda.synchronize()
     assert pkv.device_error(clear=True) == 0
-    oracle.kv_append(f16_host(kn), f16_host(vn), np.asarray(slots, np.int64), k_host, v_host, bs)
+    oracle.kv_append(f16_host(kn), f16_host(vn), slots, k_host, v_host, bs)
     assert np.array_equal(u16(k), k_host.view(np.uint16))
     assert np.array_equal(u16(v), v_host.view(np.uint16))
     ref = oracle.paged_attention(f16_host(q), k_host, v_host, bt, lens, bs, scale)
