@@ -1,16 +1,27 @@
 #!/usr/bin/env python
 """Benchmark of paged decode attention on one GPU (or N data-parallel replicas).
 
-One step is one decode step of the whole attention stack of the workload: for every layer
-one fused launch that writes the step's new K/V rows to the slots the block table maps their
-positions to (slot mapping + KV append) and runs the paged decode attention, all through the
-C ABI of libpkv.so, captured once in a CUDA graph and replayed.
+One step is one decode step of the whole attention stack of a workload, all through the C ABI
+of libpkv.so, captured once in a CUDA graph and replayed:
+  * paged GQA workloads (llama70b_b16, llama70b_mixed, edge_1p1b): per layer one fused launch
+    that writes the step's new K/V rows to the slots the block table maps their positions to
+    (slot mapping + KV append) and runs the paged decode attention;
+  * prefix: the beam fork's copy-on-write block copies, then the fused append + decode;
+  * ring: four draft tokens per sequence (sink + ring slot mapping, append, causal decode over
+    every layer), a rollback of two, then one more token (mapping, append, decode).
+
+The headline line is the largest single-GPU workload, llama70b_b16 (21.5 GB of K/V per step);
+the other workloads are measured in the same run and reported under "per_workload", each with
+its own roofline, end-to-end figure and clock record. Every timed region replays `--steps`
+steps back to back, repeated until at least `--min-seconds` of GPU time has passed; the
+median repeat is reported (ms_per_step x steps describes one repeat).
 
 Printed (rank 0, one JSON line): the KV-read bandwidth (algorithmic fp16 K+V bytes the step
 reads over the step time), decode tokens/s, the decode kernel's roofline against the
 measured HBM copy peak, the end-to-end figure with host buffers (inputs copied in and the
 attention output copied back every step), the fp64 CPU oracle's rate on a bounded sample of
-the same workload, the SM clocks seen during the timed region and the kernel launch count.
+the headline workload, the SM clocks seen during the timed regions and the kernel launch
+count.
 
 `--impl reference` times the CPU oracle alone (the reference arm): each step is a bounded
 sample of the workload, sized so the whole run ends in a few minutes.
@@ -18,6 +29,8 @@ sample of the workload, sized so the whole run ends in a few minutes.
 from __future__ import annotations
 
 import argparse
+import copy as _copy
+import gc
 import hashlib
 import json
 import math
@@ -39,19 +52,23 @@ from paged_kv_cache_147_gb300 import replicas, workloads  # noqa: E402
 METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak), decode tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
+ALL_WORKLOADS = ["llama70b_b16", "edge_1p1b", "llama70b_mixed", "prefix", "ring"]
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="edge_1p1b",
-                    choices=["edge_1p1b", "llama70b_b16", "llama70b_mixed", "prefix", "ring"],
-                    help="prefix: the shared-prefix MHA batch, decode only (its forked children "
-                         "share their last block, so there is no append); ring: the sink + "
-                         "ring cache over 24 layers, 4 draft queries per sequence")
+    ap.add_argument("--workload", default="llama70b_b16", choices=ALL_WORKLOADS,
+                    help="the headline workload (default: the largest single-GPU one)")
+    ap.add_argument("--also", default="edge_1p1b,llama70b_mixed,prefix,ring",
+                    help="comma-separated workloads measured after the headline and reported "
+                         "under per_workload ('none': headline only)")
+    ap.add_argument("--min-seconds", type=float, default=1.5,
+                    help="each timed region repeats the --steps block until it has run this "
+                         "long; the median repeat is reported")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -62,7 +79,7 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers than the workload's (small profiler captures; the "
                          "per-launch figures are unchanged, the step and the L2 note shrink)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def load_peaks():
@@ -75,16 +92,29 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def make_workload(name, layers=None):
+    # the ring cache spans 24 layers of the 1.1B shape, so that a step exceeds L2
+    w = workloads.ring(num_layers=24) if name == "ring" else workloads.WORKLOADS[name]()
+    if layers is not None:
+        w.num_layers = max(1, min(layers, w.num_layers))
+    return w
+
+
+def ring_phase_tokens(w) -> int:
+    """K/V rows one ring decode launch reads per (sequence, kv head): the slots it holds."""
+    hw = w.ring_len0.astype(np.int64) + w.q_len       # the drafts' high-water mark
+    return int(np.minimum(hw, w.sink + w.window).sum())
+
+
 def step_bytes(w, kv="fp16") -> int:
     """Algorithmic K+V bytes one step reads over all layers: every visible token of every
-    (sequence, kv head) once (for the ring, the min(hw, sink + window) slots it holds); an E4M3
-    cache holds one byte per element instead of two."""
+    (sequence, kv head) once. The ring step decodes twice per layer (the drafts, then the token
+    after the rollback), each over the min(hw, sink + window) slots it holds. An E4M3 cache
+    holds one byte per element instead of two."""
     if kv == "fp8":
         return w.kv_read_bytes() // 2
     if w.name == "ring":
-        hw = w.context_lens.astype(np.int64)          # L = hw: no rollback in this step
-        toks = int(np.minimum(hw, w.sink + w.window).sum())
-        return toks * w.num_kv_heads * w.head_dim * 2 * 2 * w.num_layers
+        return 2 * ring_phase_tokens(w) * w.num_kv_heads * w.head_dim * 2 * 2 * w.num_layers
     return w.kv_read_bytes()
 
 
@@ -140,6 +170,13 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # nvidia-smi takes a moment to start: the timed region begins once it samples
+        t_end = time.time() + 5.0
+        while time.time() < t_end and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self) -> dict | None:
         if self.proc is None:
@@ -169,16 +206,19 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------ our arm
 class Step:
-    """Device-resident inputs of one decode step and the launches that make it."""
+    """Device-resident inputs of one decode step and the launches that make it.
 
-    def __init__(self, w, dev, seed_offset=0, kv="fp16"):
+    The per-step inputs and outputs are attributes named in `in_names` / `out_names` (the
+    end-to-end measurement copies exactly those to and from the host)."""
+
+    def __init__(self, w, dev, kv="fp16"):
         from paged_kv_cache_147_gb300 import pkv
         self.pkv = pkv
         self.w = w
         self.dev = dev
-        # fused append + decode per layer (paged workloads), decode only (prefix), the sink +
-        # ring decode (ring), or FP8 append + FP8 decode per layer (an E4M3 cache)
-        self.kind = {"prefix": "decode", "ring": "ring"}.get(w.name, "fused")
+        # fused append + decode per layer (paged workloads), copy-on-write then fused (prefix),
+        # drafts / rollback / one more token (ring), or the E4M3 form of the fused step
+        self.kind = {"prefix": "prefix", "ring": "ring"}.get(w.name, "fused")
         if kv == "fp8":
             if self.kind != "fused":
                 raise SystemExit("--kv fp8 applies to the paged GQA workloads")
@@ -186,56 +226,154 @@ class Step:
         Lr = w.num_layers
         self.k, self.v = w.pools(dev)
         if self.kind == "fp8":
-            # E4M3 pools from the same data, one scale per (layer, kv head): max |x| / 448
-            k8 = torch.empty(self.k.shape, dtype=torch.uint8, device=dev)
-            v8 = torch.empty(self.v.shape, dtype=torch.uint8, device=dev)
-            self.ks = torch.empty((Lr, w.num_kv_heads), dtype=torch.float32, device=dev)
-            self.vs = torch.empty_like(self.ks)
-            for l in range(Lr):
-                for src, dst, sc in ((self.k, k8, self.ks), (self.v, v8, self.vs)):
-                    x = src[l].float()
-                    sc[l] = x.abs().amax(dim=(0, 2, 3)) / 448.0
-                    y = (x / sc[l][None, :, None, None]).clamp(-448.0, 448.0)
-                    dst[l] = y.to(torch.float8_e4m3fn).view(torch.uint8)
-            self.k, self.v = k8, v8
+            self._to_e4m3()
+        if self.kind == "prefix":
+            self._fork_tables()
         self.bt = torch.as_tensor(w.block_tables, device=dev)
         self.cl = torch.as_tensor(w.context_lens, device=dev)
+        self.q = torch.stack([w.query(l, dev) for l in range(Lr)])
+        kv_rows = [w.new_kv(l, dev) for l in range(Lr)]
+        self.kn = torch.stack([a for a, _ in kv_rows])
+        self.vn = torch.stack([b for _, b in kv_rows])
+        self.out = torch.empty_like(self.q)
         seq, pos = w.new_token_positions()
         self.seq = torch.as_tensor(seq, device=dev)
         self.pos = torch.as_tensor(pos, device=dev)
-        self.q = torch.stack([w.query(l, dev) for l in range(Lr)])
-        kv = [w.new_kv(l, dev) for l in range(Lr)]
-        self.kn = torch.stack([a for a, _ in kv])
-        self.vn = torch.stack([b for _, b in kv])
-        self.out = torch.empty_like(self.q)
         self.slots = torch.empty(seq.shape[0], dtype=torch.int64, device=dev)
         self.ws = pkv.make_workspace(w.num_seqs, w.q_len, w.num_q_heads, w.num_kv_heads, dev)
+        self.in_names = ["q", "kn", "vn", "bt", "cl"]
+        self.out_names = ["out"]
         self.launches_per_step = Lr
+        self.tokens_per_step = w.num_seqs * w.q_len
+        if self.kind == "prefix":
+            self.in_names += ["cow_src", "cow_dst"]
+            self.launches_per_step = Lr + 1
         if self.kind == "ring":
-            self.L = torch.as_tensor(w.context_lens.astype(np.int64), device=dev)
-            self.hw = self.L.clone()
-            self.rope = pkv.rope_table(w.sink + w.window).to(dev)
+            self._ring_setup()
 
+    # -- workload-specific set-up -------------------------------------------------------------
+    def _to_e4m3(self):
+        """E4M3 pools from the same data, one scale per (layer, kv head): max |x| / 448."""
+        w, dev = self.w, self.dev
+        k8 = torch.empty(self.k.shape, dtype=torch.uint8, device=dev)
+        v8 = torch.empty(self.v.shape, dtype=torch.uint8, device=dev)
+        self.ks = torch.empty((w.num_layers, w.num_kv_heads), dtype=torch.float32, device=dev)
+        self.vs = torch.empty_like(self.ks)
+        for l in range(w.num_layers):
+            for src, dst, sc in ((self.k, k8, self.ks), (self.v, v8, self.vs)):
+                x = src[l].float()
+                sc[l] = x.abs().amax(dim=(0, 2, 3)) / 448.0
+                y = (x / sc[l][None, :, None, None]).clamp(-448.0, 448.0)
+                dst[l] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+        self.k, self.v = k8, v8
+
+    def _fork_tables(self):
+        """The beam fork: children 60..63 share their parent's partly filled last block; the
+        first three writers find it shared and copy it to a spare block (copy-on-write), the
+        last writes in place. The step replays these copies and then the appends."""
+        w = self.w
+        tables = w.block_tables.copy()
+        last = (int(w.context_lens[60]) - 1) // w.block_size
+        shared = int(tables[60, last])
+        spare = list(w.free_blocks)
+        src, dst = [], []
+        for child in (60, 61, 62):
+            tables[child, last] = spare.pop(0)
+            src.append(shared)
+            dst.append(int(tables[child, last]))
+        w.block_tables = tables
+        self.cow_src = torch.tensor(src, dtype=torch.int32, device=self.dev)
+        self.cow_dst = torch.tensor(dst, dtype=torch.int32, device=self.dev)
+        self.cow_bytes = 2 * 2 * len(src) * w.num_kv_heads * w.block_size * w.head_dim * 2
+
+    def _ring_setup(self):
+        """Drafts at positions L0 .. L0+3 (hw = L = L0 + 4), then a rollback of two and one
+        more token at L0 + 2 (L = L0 + 3, hw stays L0 + 4)."""
+        w, dev, pkv = self.w, self.dev, self.pkv
+        B, nd = w.num_seqs, w.q_len
+        L0 = w.ring_len0.astype(np.int64)
+        self.pos_b = torch.as_tensor(L0 + nd - 2, device=dev)
+        self.seq_b = torch.arange(B, dtype=torch.int32, device=dev)
+        self.L_a = torch.as_tensor(L0 + nd, device=dev)
+        self.hw_a = self.L_a.clone()
+        self.L_b = torch.as_tensor(L0 + nd - 1, device=dev)
+        self.hw_b = self.hw_a.clone()
+        self.slots_b = torch.empty(B, dtype=torch.int64, device=dev)
+        self.q_b = torch.stack([w.draw((B, 1, w.num_q_heads, w.head_dim), l, 120, dev)
+                                for l in range(w.num_layers)])
+        self.kn_b = torch.stack([w.draw((B, w.num_kv_heads, w.head_dim), l, 121, dev)
+                                 for l in range(w.num_layers)])
+        self.vn_b = torch.stack([w.draw((B, w.num_kv_heads, w.head_dim), l, 122, dev)
+                                 for l in range(w.num_layers)])
+        self.out_b = torch.empty_like(self.q_b)
+        self.rope = pkv.rope_table(w.sink + w.window).to(dev)
+        self.in_names = ["q", "kn", "vn", "bt", "seq", "pos", "L_a", "hw_a", "q_b", "kn_b",
+                         "vn_b", "seq_b", "pos_b", "L_b", "hw_b"]
+        self.out_names = ["out", "out_b"]
+        self.launches_per_step = 2 + 4 * w.num_layers
+        self.tokens_per_step = B * (nd + 1)
+
+    # -- the step ---------------------------------------------------------------------------------
     def run(self):
-        """One decode step: per layer, the fused call appends the new K/V rows at the slots the
-        block table gives (slot mapping + append) and runs paged decode attention."""
         p, w = self.pkv, self.w
-        if self.kind == "decode":
-            return self.run_decode_only()
-        if self.kind == "fp8":
-            for l in range(w.num_layers):
+        if self.kind == "ring":
+            return self.run_ring(decode=True, append=True)
+        if self.kind == "prefix":
+            # the copies write the pools the fused call reads: it must not start early
+            p.copy_blocks(self.k, self.v, self.cow_src, self.cow_dst)
+            prev = p.set_early_start(False)
+        for l in range(w.num_layers):
+            if self.kind == "fp8":
                 p.paged_attn_decode_append_fp8(self.out[l], self.q[l], self.kn[l], self.vn[l],
                                                self.k[l], self.v[l], self.ks[l], self.vs[l],
                                                self.bt, self.cl, w.scale, self.ws)
-            return
-        for l in range(w.num_layers):
-            if self.kind == "ring":
-                p.ring_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.L,
-                                   self.hw, w.sink, w.window, self.rope, w.scale, self.ws)
             else:
                 p.paged_attn_decode_append(self.out[l], self.q[l], self.kn[l], self.vn[l],
                                            self.k[l], self.v[l], self.bt, self.cl, w.scale,
                                            self.ws)
+        if self.kind == "prefix":
+            p.set_early_start(prev)
+
+    def run_ring(self, decode=True, append=True):
+        """The streaming step: the drafts through every layer, the rollback (host state: the
+        second phase's lengths), then one more token through every layer."""
+        p, w = self.pkv, self.w
+        if append:
+            p.ring_slot_mapping(self.seq, self.pos, self.bt, w.sink, w.window, w.block_size,
+                                out=self.slots)
+        for l in range(w.num_layers):
+            if append:
+                p.kv_append(self.kn[l], self.vn[l], self.slots, self.k[l], self.v[l])
+            if decode:
+                p.ring_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt,
+                                   self.L_a, self.hw_a, w.sink, w.window, self.rope, w.scale,
+                                   self.ws)
+        if append:
+            p.ring_slot_mapping(self.seq_b, self.pos_b, self.bt, w.sink, w.window,
+                                w.block_size, out=self.slots_b)
+        for l in range(w.num_layers):
+            if append:
+                p.kv_append(self.kn_b[l], self.vn_b[l], self.slots_b, self.k[l], self.v[l])
+            if decode:
+                p.ring_attn_decode(self.out_b[l], self.q_b[l], self.k[l], self.v[l], self.bt,
+                                   self.L_b, self.hw_b, w.sink, w.window, self.rope, w.scale,
+                                   self.ws)
+
+    def run_roofline(self):
+        """The dominant kernel's launches alone: the fused (or ring) decode launches."""
+        if self.kind == "ring":
+            return self.run_ring(decode=True, append=False)
+        if self.kind == "prefix":
+            p, w = self.pkv, self.w
+            for l in range(w.num_layers):
+                p.paged_attn_decode_append(self.out[l], self.q[l], self.kn[l], self.vn[l],
+                                           self.k[l], self.v[l], self.bt, self.cl, w.scale,
+                                           self.ws)
+            return
+        return self.run()
+
+    def roofline_launches(self) -> int:
+        return 2 * self.w.num_layers if self.kind == "ring" else self.w.num_layers
 
     def run_append_only(self):
         """The standalone KV append of the step (slot mapping once, then one append per
@@ -247,31 +385,24 @@ class Step:
 
     def run_decode_only(self):
         p, w = self.pkv, self.w
-        if self.kind == "ring":
-            return self.run()
-        if self.kind == "fp8":
-            for l in range(w.num_layers):
+        for l in range(w.num_layers):
+            if self.kind == "fp8":
                 p.paged_attn_decode_fp8(self.out[l], self.q[l], self.k[l], self.v[l],
                                         self.ks[l], self.vs[l], self.bt, self.cl, w.scale,
                                         self.ws)
-            return
-        for l in range(w.num_layers):
-            p.paged_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.cl,
-                                w.scale, self.ws)
-
-    def h2d_sources(self):
-        if self.kind == "decode":
-            return [self.q, self.bt, self.cl]
-        if self.kind == "ring":
-            return [self.q, self.bt, self.L, self.hw]
-        return [self.q, self.kn, self.vn, self.bt, self.cl, self.seq, self.pos]
+            else:
+                p.paged_attn_decode(self.out[l], self.q[l], self.k[l], self.v[l], self.bt,
+                                    self.cl, w.scale, self.ws)
 
     def graph_note(self) -> str:
         n = self.w.num_layers
-        if self.kind == "decode":
-            return f"CUDA graph: {n} x paged_attn_decode (decode only)"
         if self.kind == "ring":
-            return f"CUDA graph: {n} x ring_attn_decode ({self.w.q_len} causal draft queries)"
+            return (f"CUDA graph: ring_slot_mapping, {n} x (kv_append + ring_attn_decode of "
+                    f"{self.w.q_len} causal drafts); rollback 2; ring_slot_mapping, {n} x "
+                    "(kv_append + ring_attn_decode of 1 token)")
+        if self.kind == "prefix":
+            return (f"CUDA graph: copy_blocks (3 copy-on-write copies of the forked children's "
+                    f"shared block), {n} x paged_attn_decode_append")
         if self.kind == "fp8":
             return (f"CUDA graph: {n} x paged_attn_decode_append_fp8 "
                     "(slot mapping + E4M3 append + decode, one launch)")
@@ -279,8 +410,7 @@ class Step:
                 "(slot mapping + KV append + decode, one launch)")
 
     def kernel_note(self) -> str:
-        return {"decode": "decode_kernel (paged_attn_decode)",
-                "fp8": "decode_kernel, E4M3 cache, fused append (paged_attn_decode_append_fp8)",
+        return {"fp8": "decode_kernel, E4M3 cache, fused append (paged_attn_decode_append_fp8)",
                 "ring": "decode_kernel, sink + ring with RoPE on read (ring_attn_decode)"}.get(
             self.kind, "decode_kernel, fused append (paged_attn_decode_append)")
 
@@ -299,20 +429,41 @@ def capture(fn):
     return g
 
 
-def time_replays(g, steps, warmup) -> float:
-    for _ in range(warmup):
-        g.replay()
+def time_repeats(run_block, warmup_block, min_s, clocks=None):
+    """Runs warmup_block() once, then run_block() (one block of --steps steps) repeatedly,
+    back to back, until at least min_s seconds of GPU time have passed (at least 3 repeats),
+    timing each repeat with CUDA events on the current stream. Returns (median repeat
+    seconds, repeats, total seconds, clocks)."""
+    warmup_block()
     torch.cuda.synchronize()
     replicas.barrier()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        g.replay()
-    end.record()
-    end.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    run_block()                      # sizes the repeat count (not reported)
+    t1.record()
+    t1.synchronize()
+    once = max(t0.elapsed_time(t1) / 1e3, 1e-6)
+    n = max(3, math.ceil(min_s / once))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    if clocks is not None:
+        clocks.start()
+    ev[0].record()
+    for i in range(n):
+        run_block()
+        ev[i + 1].record()
+    ev[-1].synchronize()
     torch.cuda.synchronize()
+    clk = clocks.stop() if clocks is not None else None
     replicas.barrier()
-    return start.elapsed_time(end) / 1e3
+    per = [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(n)]
+    return statistics.median(per), n, sum(per), clk
+
+
+def time_graph(g, steps, warmup, min_s, clocks=None):
+    def block(k=steps):
+        for _ in range(k):
+            g.replay()
+    return time_repeats(block, lambda: block(warmup), min_s, clocks)
 
 
 def traffic_record(w):
@@ -330,52 +481,38 @@ def traffic_record(w):
     return None
 
 
-def measure_e2e(st, step_graph, args, bytes_step, dev):
+def measure_e2e(st, step_graph, args, bytes_step, dev, local_rank):
     """The step through the public API with its host traffic: every step copies its inputs from
     pinned host memory to the device and reads its attention output back. Measured twice:
     serially on one stream, and as a serving loop would run it, double-buffered (step i+1's
     inputs go up and step i's output comes down on copy streams while step i's kernels run).
-    The pipelined figure is the reported value; the serial one is kept beside it."""
-    import copy as _copy
-    srcs = st.h2d_sources()
-    host_in = [t.cpu().pin_memory() for t in srcs]
-    host_out = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(2)]
+    Both are timed over the same repeated blocks of --steps steps as the device figure; the
+    pipelined figure is the reported value, the serial one is kept beside it."""
+    ins = [getattr(st, n) for n in st.in_names]
+    outs = [getattr(st, n) for n in st.out_names]
+    host_in = [t.cpu().pin_memory() for t in ins]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+                for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_out[0].numel() * host_out[0].element_size()
-    esteps = max(5, args.steps // 10)
-    warm = max(3, args.warmup // 3)
-
-    def timed(run_steps):
-        torch.cuda.synchronize()
-        replicas.barrier()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record()
-        run_steps(esteps)
-        t1.record()
-        t1.synchronize()
-        el, nbytes = replicas.aggregate(t0.elapsed_time(t1) / 1e3, float(bytes_step) * esteps,
-                                        device=dev)
-        return el, nbytes
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
 
     # serial: copy in, step, copy out, one stream
     def serial(n):
         for _ in range(n):
-            for d, h in zip(srcs, host_in):
+            for d, h in zip(ins, host_in):
                 d.copy_(h, non_blocking=True)
             step_graph.replay()
-            host_out[0].copy_(st.out, non_blocking=True)
+            for h, d in zip(host_out[0], outs):
+                h.copy_(d, non_blocking=True)
 
-    serial(warm)
-    s_el, s_bytes = timed(serial)
+    s_med, s_rep, _, _ = time_repeats(lambda: serial(args.steps), lambda: serial(args.warmup),
+                                      args.min_seconds)
 
     # double-buffered: a second set of input / output buffers (same pools and workspace) and
     # its own graph; the copy streams overlap the other set's kernels
     st2 = _copy.copy(st)
-    for name in ("q", "kn", "vn", "bt", "cl", "seq", "pos", "L", "hw"):
-        if hasattr(st, name):
-            setattr(st2, name, getattr(st, name).clone())
-    st2.out = torch.empty_like(st.out)
+    for name in st.in_names + st.out_names:
+        setattr(st2, name, getattr(st, name).clone())
     sets = [st, st2]
     graphs = [step_graph, capture(st2.run)]
     comp, cin, cout = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
@@ -385,8 +522,8 @@ def measure_e2e(st, step_graph, args, bytes_step, dev):
 
     def upload(sidx):
         with torch.cuda.stream(cin):
-            for d, h in zip(sets[sidx].h2d_sources(), host_in):
-                d.copy_(h, non_blocking=True)
+            for n, h in zip(st.in_names, host_in):
+                getattr(sets[sidx], n).copy_(h, non_blocking=True)
             ev_in[sidx].record(cin)
 
     def pipelined(n):
@@ -406,93 +543,137 @@ def measure_e2e(st, step_graph, args, bytes_step, dev):
                 upload(1 - sidx)
             cout.wait_event(ev_comp[sidx])
             with torch.cuda.stream(cout):
-                host_out[sidx].copy_(sets[sidx].out, non_blocking=True)
+                for h, name in zip(host_out[sidx], st.out_names):
+                    h.copy_(getattr(sets[sidx], name), non_blocking=True)
                 ev_out[sidx].record(cout)
         for sm in (comp, cin, cout):
             main.wait_stream(sm)
 
-    pipelined(warm)
-    p_el, p_bytes = timed(pipelined)
+    clocks = ClockSampler(local_rank)
+    p_med, p_rep, _, clk = time_repeats(lambda: pipelined(args.steps),
+                                        lambda: pipelined(args.warmup), args.min_seconds, clocks)
+    p_el, p_bytes = replicas.aggregate(p_med, float(bytes_step) * args.steps, device=dev)
+    s_el, s_bytes = replicas.aggregate(s_med, float(bytes_step) * args.steps, device=dev)
     return {"value": round(p_bytes / p_el / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": round(p_el / esteps * 1e3, 4),
+            "ms_per_step": round(p_el / args.steps * 1e3, 4), "repeats": p_rep,
             "serial_value": round(s_bytes / s_el / 1e9, 2),
-            "serial_ms_per_step": round(s_el / esteps * 1e3, 4),
+            "serial_ms_per_step": round(s_el / args.steps * 1e3, 4), "serial_repeats": s_rep,
+            "clocks": clk,
             "path": "pinned host inputs -> device, C-ABI step (graph replay), attention output "
                     "-> pinned host; double-buffered: step i+1's inputs and step i's output "
                     "move on copy streams during step i (serial_value: one stream, no overlap)"}
 
 
-def run_ours(args, w, rank, local_rank, world_size):
+def measure_workload(args, w, local_rank, world_size, kv="fp16"):
+    """Every figure of one workload: the step, the dominant kernel's roofline, the standalone
+    decode and append, and the end-to-end step."""
     dev = f"cuda:{local_rank}"
-    torch.cuda.set_device(local_rank)
     from paged_kv_cache_147_gb300 import pkv
-    pkv.load()
-    st = Step(w, dev, kv=args.kv)
+    st = Step(w, dev, kv=kv)
     step_graph = capture(st.run)
-    decode_graph = capture(st.run_decode_only)
+    steps, min_s = args.steps, args.min_seconds
 
     clocks = ClockSampler(local_rank)
-    clocks.start()
-    elapsed = time_replays(step_graph, args.steps, args.warmup)
-    clk = clocks.stop()
-    bytes_step = step_bytes(w, args.kv)
-    t_max, total_bytes = replicas.aggregate(elapsed, float(bytes_step) * args.steps,
-                                            device=dev)
+    med, reps, _, clk = time_graph(step_graph, steps, args.warmup, min_s, clocks)
+    bytes_step = step_bytes(w, kv)
+    t_max, total_bytes = replicas.aggregate(med, float(bytes_step) * steps, device=dev)
     value = total_bytes / t_max / 1e9
 
-    # dominant kernel: the decode launch is the whole step; its average launch duration is
-    # the step time over its launches (they run back to back, the fused ones each overlapping
-    # the previous one's tail). The unfused decode is timed alone as well. For the prefix batch
-    # the roofline counts the distinct block rows (the shared prefix once). With the E4M3
-    # cache the fused launch appends and decodes; the decode alone is
-    # unfused_decode_launch_us.
-    per_launch = (t_max / args.steps) / w.num_layers
-    bytes_launch = (unique_bytes(w) if w.name == "prefix" else bytes_step) / w.num_layers
+    # dominant kernel: the decode launches. For the paged workloads they are the whole step
+    # (the fused ones each overlapping the previous one's tail), so their average launch
+    # duration is the step time over the launches. The prefix step also holds the copy-on-write
+    # copies, the ring step its slot mappings and appends: there the decode launches are timed
+    # alone. The prefix roofline counts the distinct block rows (the shared prefix once).
+    nroof = st.roofline_launches()
+    if st.kind in ("fused", "fp8"):
+        per_launch = (t_max / steps) / nroof
+    else:
+        roof_graph = capture(st.run_roofline)
+        r_med, _, _, _ = time_graph(roof_graph, steps, args.warmup, min_s / 2)
+        per_launch = r_med / steps / nroof
+    if w.name == "prefix":
+        bytes_launch = unique_bytes(w) / w.num_layers
+    else:
+        bytes_launch = bytes_step / nroof
     peak, peak_kind = load_peaks()
     achieved = bytes_launch / per_launch / 1e9
-    traffic = traffic_record(w) if args.kv == "fp16" else None
-    dsteps = max(10, args.steps // 2)
-    plain_per_launch = time_replays(decode_graph, dsteps, args.warmup) / (dsteps * w.num_layers)
-    append_per_launch = None
-    if st.kind == "fused":
-        append_graph = capture(st.run_append_only)
-        append_per_launch = time_replays(append_graph, dsteps, args.warmup) / (dsteps * w.num_layers)
+    traffic = traffic_record(w) if kv == "fp16" else None
+
+    extra = {}
+    if st.kind in ("fused", "fp8", "prefix"):
+        dg = capture(st.run_decode_only)
+        d_med, _, _, _ = time_graph(dg, steps, args.warmup, min_s / 4)
+        extra["unfused_decode_launch_us"] = round(d_med / steps / w.num_layers * 1e6, 3)
+    if st.kind in ("fused", "prefix"):
+        ag = capture(st.run_append_only)
+        a_med, _, _, _ = time_graph(ag, steps, args.warmup, min_s / 4)
+        extra["standalone_kv_append_launch_us"] = round(a_med / steps / w.num_layers * 1e6, 3)
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(st, step_graph, args, bytes_step, dev)
+        e2e = measure_e2e(st, step_graph, args, bytes_step, dev, local_rank)
     dev_err = pkv.device_error(clear=True)
     if dev_err:
-        raise RuntimeError(f"device error word {dev_err:#x} after the benchmark")
+        raise RuntimeError(f"device error word {dev_err:#x} after the {w.name} benchmark")
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world_size,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(t_max / args.steps * 1e3, 4), "higher_is_better": True,
+        "steps": steps, "warmup": args.warmup, "repeats": reps,
+        "ms_per_step": round(t_max / steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 K/V, f16 q/out" if args.kv == "fp8" else "f16", "data": "synthetic",
-        "config": describe(w, args.kv) | {"graph": st.graph_note(), "kv": args.kv,
-                                 "parallelism": f"replicas x{world_size}"},
-        "decode_tokens_per_s": round(w.num_seqs * w.q_len * args.steps * world_size / t_max, 1),
+        "dtype": "e4m3 K/V, f16 q/out" if kv == "fp8" else "f16", "data": "synthetic",
+        "config": describe(w, kv) | {"graph": st.graph_note(), "kv": kv,
+                                     "parallelism": f"replicas x{world_size}",
+                                     "timing": f"median of {reps} repeats of {steps} graph "
+                                               f"replays (>= {min_s:g} s of GPU time)"},
+        "decode_tokens_per_s": round(st.tokens_per_step * steps * world_size / t_max, 1),
         "pct_of_nominal_8tbs": round(100 * value / world_size / NOMINAL_HBM_GBS, 2),
         f"pct_of_{peak_kind}_hbm": round(100 * value / world_size / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": st.kernel_note(),
                      "launch_us": round(per_launch * 1e6, 3),
-                     "unfused_decode_launch_us": round(plain_per_launch * 1e6, 3),
-                     "standalone_kv_append_launch_us":
-                         None if append_per_launch is None else round(append_per_launch * 1e6, 3),
                      "algorithmic_bytes_per_launch": int(bytes_launch),
-                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)", **extra},
         "e2e": e2e,
-        "gpu_launches": st.launches_per_step * args.steps,
-        **({"unique_kv_bytes_per_step": unique_bytes(w),
-            "unique_gbs": round(unique_bytes(w) * args.steps * world_size / t_max / 1e9, 2)}
-           if w.name == "prefix" else {}),
+        "gpu_launches": st.launches_per_step * steps * reps,
         "clocks": clk,
     }
+    if w.name == "prefix":
+        ub = unique_bytes(w)
+        line["unique_kv_bytes_per_step"] = ub
+        line["unique_gbs"] = round(ub * steps * world_size / t_max / 1e9, 2)
+        line["cow_copy_bytes_per_step"] = st.cow_bytes
+    del st, step_graph
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_ours(args, w, rank, local_rank, world_size):
+    torch.cuda.set_device(local_rank)
+    from paged_kv_cache_147_gb300 import pkv
+    pkv.load()
+    line = measure_workload(args, w, local_rank, world_size, args.kv)
+    also = [] if args.also in ("", "none") else [x for x in args.also.split(",") if x]
+    per = []
+    for name in also:
+        if name == w.name or name not in ALL_WORKLOADS:
+            continue
+        if args.kv == "fp8" and name in ("prefix", "ring"):
+            continue
+        gc.collect()
+        torch.cuda.empty_cache()
+        wx = make_workload(name, args.layers)
+        entry = measure_workload(args, wx, local_rank, world_size, args.kv)
+        for key in ("metric", "n_gpus", "higher_is_better", "scaling", "data", "vs_baseline"):
+            entry.pop(key, None)
+        per.append(entry)
+    if per:
+        line["per_workload"] = per
+        line["gpu_launches_all_workloads"] = line["gpu_launches"] + sum(
+            e["gpu_launches"] for e in per)
     return line
 
 
@@ -533,19 +714,23 @@ def oracle_sample(w, seqs, layers):
     return secs, nbytes, threads
 
 
-def cpu_baseline(w, budget_s):
+def cpu_baseline(w, budget_s, max_layers=4):
+    """The oracle as it stands on all host cores: whole layers of the workload (all sequences,
+    append + fp64 attention), cycling over its first max_layers layers (host copies of every
+    layer of the 80-layer batches would not fit the host's memory) for about budget_s."""
     import oracle
     oracle.build()
+    nl = min(w.num_layers, max_layers)
     secs, nbytes, threads = oracle_sample(w, range(w.num_seqs), [0])
-    layers = 1   # layer evaluations, cycling over the workload's layers
+    layers = 1   # layer evaluations
     while secs * (layers + 1) / layers < budget_s:
-        s, b, threads = oracle_sample(w, range(w.num_seqs), [layers % w.num_layers])
+        s, b, threads = oracle_sample(w, range(w.num_seqs), [layers % nl])
         secs, nbytes, layers = secs + s, nbytes + b, layers + 1
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"{layers} layer evaluations ({layers / w.num_layers:.1f} passes over the "
-                      f"{w.num_layers} layers), all {w.num_seqs} sequences (append + fp64 "
-                      f"attention), {secs:.1f} s"}
+            "sample": f"{layers} layer evaluations cycling over layers 0-{nl - 1} of "
+                      f"{w.name}, all {w.num_seqs} sequences (append + fp64 attention), "
+                      f"{secs:.1f} s"}
 
 
 def run_reference(args, w, world_size):
@@ -582,11 +767,7 @@ def run_reference(args, w, world_size):
 def main():
     args = parse_args()
     rank, local_rank, world_size = replicas.world()
-    # the ring cache spans 24 layers of the 1.1B shape, so that a step exceeds L2
-    w = workloads.ring(num_layers=24) if args.workload == "ring" else \
-        workloads.WORKLOADS[args.workload]()
-    if args.layers is not None:
-        w.num_layers = max(1, min(args.layers, w.num_layers))
+    w = make_workload(args.workload, args.layers)
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w, world_size)), flush=True)

@@ -28,7 +28,7 @@ SYMBOLS = (
     "pkv_kv_append_fp8", "pkv_paged_attn_decode_fp8", "pkv_paged_attn_decode_append_fp8",
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocate", "pkv_pool_warm",
     "pkv_pool_release", "pkv_pool_fork", "pkv_pool_append", "pkv_pool_stats",
-    "pkv_pool_refcount", "pkv_spec_verify",
+    "pkv_pool_refcount", "pkv_spec_verify", "pkv_set_early_start",
 )
 
 OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
@@ -100,6 +100,7 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
                                             i32, i32, i32, f32, P, sz, P]),
         "pkv_paged_attn_decode_append_fp8": (i32, [P, P, P, P, P, P, P, P, i32, P, i32, P, i32,
                                                    i32, i32, i32, i32, i32, f32, P, sz, P]),
+        "pkv_set_early_start": (i32, [i32]),
         "pkv_pool_create": (i32, [i32, i32, i32, P]),
         "pkv_pool_destroy": (None, [P]),
         "pkv_pool_allocate": (i32, [P, P, i32, i32, P, i32, P, P]),
@@ -191,6 +192,12 @@ def copy_blocks(k_cache, v_cache, src, dst, stream=None):
 
 
 # ------------------------------------------------------------------------------ attention
+def set_early_start(enable: bool) -> bool:
+    """Lets the fused-append calls start while the previous kernel finishes (True, the
+    default) or not; returns the previous setting. Process-wide."""
+    return bool(load().pkv_set_early_start(1 if enable else 0))
+
+
 def decode_workspace_bytes(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim=128) -> int:
     n = load().pkv_decode_workspace_bytes(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim)
     if n == 0:
@@ -254,7 +261,12 @@ def paged_attn_decode_append_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale
 def paged_attn_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
                              scale, workspace, stream=None):
     """Decode step with the KV append fused in: k_new, v_new [B*q_len, Hkv, D] go to the slots of
-    positions context_lens[b] - q_len + i, then attention runs over the cache including them."""
+    positions context_lens[b] - q_len + i, then attention runs over the cache including them.
+
+    WARNING: by default this launch may start before the kernel ahead of it on the stream has
+    finished, and it reads the K/V pools, block_tables and context_lens early. If the kernel
+    right before it writes any of those (a torch op that advances context_lens, copy_blocks,
+    ...), put another launch or a copy in between, or call set_early_start(False) first."""
     B, q_len, hq, d = q.shape
     nb, hkv, bs, _ = k_cache.shape
     _check("pkv_paged_attn_decode_append", load().pkv_paged_attn_decode_append(

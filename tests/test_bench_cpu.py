@@ -21,6 +21,6 @@ def test_reference_arm_prints_one_contract_line():
                 "cpu_baseline", "e2e"):
         assert key in d, key
     assert d["impl"] == "reference" and d["steps"] == 1 and d["n_gpus"] == 1
-    assert d["config"]["workload"] == "edge_1p1b" and d["value"] > 0
+    assert d["config"]["workload"] == "llama70b_b16" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
