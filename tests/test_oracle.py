@@ -267,6 +267,44 @@ def test_paged_attention_causal_multi_query_matches_sdpa():
     assert np.max(np.abs(got - ref)) < 1e-12
 
 
+@pytest.mark.parametrize("q_len,hq,bs", [(37, 16, 16), (64, 12, 16), (101, 16, 64)])
+def test_paged_attention_prefill_chunk_matches_sdpa(q_len, hq, bs):
+    """A chunk of q_len new queries over a paged cache (the chunked-prefill shape): query i sees
+    positions [0, ctx - q_len + i]; a query with no visible position (q_len > ctx) gives 0."""
+    rng = np.random.default_rng(q_len)
+    lens = np.array([38, 101, 20], dtype=np.int32)
+    nblk = [(int(n) + bs - 1) // bs for n in lens]
+    perm = rng.permutation(sum(nblk) + 3).astype(np.int32)
+    tables = np.full((3, max(nblk)), -1, np.int32)
+    cur = 0
+    for b, n in enumerate(nblk):
+        tables[b, :n] = perm[cur:cur + n]
+        cur += n
+    nb = len(perm)
+    k = rng.standard_normal((nb, 2, bs, 128)).astype(np.float16)
+    v = rng.standard_normal((nb, 2, bs, 128)).astype(np.float16)
+    q = rng.standard_normal((3, q_len, hq, 128)).astype(np.float16)
+    scale = 0.0883
+    got = oracle.paged_attention(q, k, v, tables, lens, bs, scale)
+    G = hq // 2
+    for b in range(3):
+        ctx = int(lens[b])
+        slots = _enumerated_slots(tables[b], nblk[b], bs)[:ctx]
+        K = k[np.array(slots) // bs, :, np.array(slots) % bs, :].astype(np.float64)
+        V = v[np.array(slots) // bs, :, np.array(slots) % bs, :].astype(np.float64)
+        Kt = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        Vt = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        for i in range(q_len):
+            vis = ctx - q_len + i + 1
+            if vis <= 0:
+                assert np.all(got[b, i] == 0.0)
+                continue
+            Qt = torch.from_numpy(q[b, i].astype(np.float64))[:, None, :]        # [Hq, 1, D]
+            o = torch.nn.functional.scaled_dot_product_attention(
+                Qt, Kt[:, :vis], Vt[:, :vis], scale=scale)
+            assert np.max(np.abs(got[b, i] - o[:, 0].numpy())) < 1e-12, (b, i)
+
+
 def test_single_token_context_returns_v():
     w, q, k, v = _tiny_inputs(poison=False)
     lens = np.array([1, 1], dtype=np.int32)
