@@ -181,6 +181,24 @@ int pkv_paged_attn_decode_append(void* out, const void* q, const void* k_new, co
                                  float scale, void* workspace, size_t workspace_bytes,
                                  pkv_stream_t stream);
 
+/* Chunked-prefill paged attention ([VLLM] §工程权衡, chunked prefill: a long prompt is processed
+ * in chunks, each attending over the paged cache that already holds the earlier chunks). The
+ * operation is pkv_paged_attn_decode's with a long query chunk: for sequence b, chunk token
+ * i < q_len at position p = context_lens[b] - q_len + i and query head h (kv head h / G),
+ *   out[b][i][h][:] = softmax_t(scale * <q[b][i][h], K_t>) . V,   t <= p   (causal),
+ * with K_t, V_t read through the block table. context_lens count the tokens in cache including
+ * the chunk, whose K/V rows must already be in the pools (pkv_kv_append first). A query with no
+ * visible token (p < 0) gets zeros. q, out (device): fp16 [num_seqs][q_len][num_q_heads]
+ * [head_dim]; caches, tables and lengths as for pkv_paged_attn_decode. Runs on the tensor
+ * cores (tcgen05, f16 operands, f32 accumulation); needs no workspace. Requires
+ * num_q_heads / num_kv_heads <= 128. The result is bit-identical for identical inputs and does
+ * not depend on which physical blocks hold the data. */
+int pkv_paged_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      int num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int num_seqs, int q_len, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, float scale,
+                      pkv_stream_t stream);
+
 /* Paged decode attention for callers that cannot allocate device memory: the same operation,
  * arguments and result as pkv_paged_attn_decode, with the scratch (arrival counters and
  * split-context partials) taken from a fixed array inside the library instead of a caller

@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkv.so")
-SOURCES = ["pkv_decode.cu", "pkv_cache.cu", "pkv_host.cu", "pkv_blocks.cpp", "pkv_spec.cu"]
+SOURCES = ["pkv_decode.cu", "pkv_cache.cu", "pkv_host.cu", "pkv_blocks.cpp", "pkv_spec.cu",
+           "pkv_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-diag-suppress", "177"]

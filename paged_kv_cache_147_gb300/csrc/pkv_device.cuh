@@ -224,6 +224,23 @@ __device__ __forceinline__ uint64_t global_time_ns() {
   return t;
 }
 
+// mbar_wait bounded in time rather than in polls (a try_wait may suspend the thread for a
+// while before it returns false): gives up after limit_ns of the GPU's global timer, or soon
+// after *abort is set.
+__device__ __forceinline__ bool mbar_wait_ns(uint32_t bar, uint32_t parity,
+                                             const volatile int* abort, uint64_t limit_ns) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (abort && *abort) return false;
+      const uint64_t now = global_time_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > limit_ns) return false;
+    }
+  }
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -244,5 +261,101 @@ __device__ __forceinline__ void cp_async_wait_all() {
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t c8) {
   return row * 128u + ((c8 ^ (row & 7u)) << 4);
 }
+
+// ---- 5th-generation tensor cores (tcgen05) and tensor memory (TMEM) --------------------------
+// Allocation of `ncols` TMEM columns (a power of two >= 32) by one whole warp; the base
+// address is written to shared memory at `dst`. The permit is given up at once so that other
+// CTAs on the SM may allocate too.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               ::"r"(dst), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Ordering of tcgen05 operations against thread synchronisation (barriers, mbarriers).
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// The mbarrier at `bar` gets one arrival when every tcgen05.mma this thread issued so far has
+// completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(bar) : "memory");
+}
+// D(TMEM, f32) = A(smem) * B(smem) (+ D when accumulate != 0), kind::f16, one CTA.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Instruction descriptor of kind::f16 with f16 A and B and an f32 accumulator: M x N tile,
+// A K-major, B K-major (b_mn_major = false) or MN-major.
+__host__ __device__ constexpr uint32_t tc_idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4)                                   // D format: f32
+         | (0u << 7) | (0u << 10)                    // A, B format: f16
+         | (0u << 15)                                // A K-major
+         | (static_cast<uint32_t>(b_mn_major) << 16)  // B major-ness
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand (atoms of 8 rows x 128 bytes,
+// 1024-byte aligned): start address, leading and stride byte offsets.
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+         (static_cast<uint64_t>(1) << 46) |          // descriptor version (fixed 0b001)
+         (static_cast<uint64_t>(2) << 61);           // 128-byte swizzle
+}
+
+#define PKV_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define PKV_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
+                  "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane (warp w reads lanes 32 (w % 4) ..
+// + 31; taddr carries the lane in its upper half), waited for before returning.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31}, [%32];\n\ttcgen05.wait::ld.sync.aligned;"
+      : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+// 64 columns in two loads and one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, "
+      "%41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, "
+      "%59, %60, %61, %62, %63}, [%65];\n\ttcgen05.wait::ld.sync.aligned;"
+      : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24), PKV_R8(32), PKV_R8(40), PKV_R8(48),
+        PKV_R8(56)
+      : "r"(taddr), "r"(taddr + 32)
+      : "memory");
+}
+// Writes 32 columns of this thread's lane and waits until the write is done.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};\n\ttcgen05.wait::st.sync.aligned;"
+      ::"r"(taddr), PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24)
+      : "memory");
+}
+#undef PKV_R8
+#undef PKV_W8
 
 }  // namespace pkv

@@ -28,7 +28,7 @@ SYMBOLS = (
     "pkv_kv_append_fp8", "pkv_paged_attn_decode_fp8", "pkv_paged_attn_decode_append_fp8",
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocate", "pkv_pool_warm",
     "pkv_pool_release", "pkv_pool_fork", "pkv_pool_append", "pkv_pool_stats",
-    "pkv_pool_refcount", "pkv_spec_verify", "pkv_set_early_start",
+    "pkv_pool_refcount", "pkv_spec_verify", "pkv_set_early_start", "pkv_paged_prefill",
 )
 
 OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
@@ -101,6 +101,8 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
         "pkv_paged_attn_decode_append_fp8": (i32, [P, P, P, P, P, P, P, P, i32, P, i32, P, i32,
                                                    i32, i32, i32, i32, i32, f32, P, sz, P]),
         "pkv_set_early_start": (i32, [i32]),
+        "pkv_paged_prefill": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32, i32, f32,
+                                    P]),
         "pkv_pool_create": (i32, [i32, i32, i32, P]),
         "pkv_pool_destroy": (None, [P]),
         "pkv_pool_allocate": (i32, [P, P, i32, i32, P, i32, P, P]),
@@ -273,6 +275,18 @@ def paged_attn_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_table
         _p(out), _p(q), _p(k_new), _p(v_new), _p(k_cache), _p(v_cache), nb, _p(block_tables),
         block_tables.shape[1], _p(context_lens), B, q_len, hq, hkv, d, bs, float(scale),
         _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def paged_prefill(out, q, k_cache, v_cache, block_tables, context_lens, scale, stream=None):
+    """Chunked-prefill attention: q, out [B, q_len, Hq, D]; the chunk's K/V rows are already in
+    the one-layer caches [NB, Hkv, bs, D]; query i of sequence b attends causally up to position
+    context_lens[b] - q_len + i."""
+    B, q_len, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_paged_prefill", load().pkv_paged_prefill(
+        _p(out), _p(q), _p(k_cache), _p(v_cache), nb, _p(block_tables), block_tables.shape[1],
+        _p(context_lens), B, q_len, hq, hkv, d, bs, float(scale), _stream(stream)))
     return out
 
 

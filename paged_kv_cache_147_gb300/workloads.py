@@ -21,6 +21,10 @@ Recipes (the shapes follow the workloads the pages discuss):
                start with the same 4 blocks (256 shared tokens) and continue with private
                suffixes of U_int[32, 1024] tokens; sequences 60..63 are the four children of
                one forked parent whose partly filled last block they share.
+* ``prefill_70b`` a chunked-prefill step of the 70B-class stack (the vLLM memory page's
+               chunked prefill): 64 q / 8 KV heads, d 128, 16-token blocks, 16 sequences whose
+               512-token chunk ends at context 4096 (3584 tokens cached before it), 4 layers.
+               ``prefill(...)`` builds smaller chunked-prefill cases with given lengths.
 * ``ring``     sink + ring streaming cache: 12 q / 2 KV heads, d 128, 16-token blocks, sink
                4, window 1020 (64 shuffled blocks per sequence), 32 sequences at logical
                lengths U_int[2000, 100000] (every ring slot holds data).
@@ -254,6 +258,22 @@ def prefix(seed: int = 3) -> Workload:
     return Workload("prefix", seed, 1, 32, 32, 128, bs, total, 1, lens, tables, fill, free, ref)
 
 
+def prefill(seed: int, lens, q_len: int, num_q_heads: int, num_kv_heads: int,
+            block_size: int = 16, num_layers: int = 1, name: str = "prefill") -> Workload:
+    """A chunk of q_len new tokens per sequence; lens are the context lengths including the
+    chunk (a length below q_len leaves the chunk's first queries with nothing to see)."""
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, dtype=np.int32)
+    max_blocks = int((lens.max() + block_size - 1) // block_size) + 1
+    nb, tables, fill, free, ref = _allocate(rng, lens, q_len, block_size, max_blocks, spare=2)
+    return Workload(name, seed, num_layers, num_q_heads, num_kv_heads, 128, block_size, nb,
+                    q_len, lens, tables, fill, free, ref)
+
+
+def prefill_70b(seed: int = 5, num_layers: int = 4) -> Workload:
+    return prefill(seed, [4096] * 16, 512, 64, 8, 16, num_layers, name="prefill_70b")
+
+
 def ring(seed: int = 4, num_seqs: int = 32, num_layers: int = 1, q_len: int = 4) -> Workload:
     """Sink + ring cache; ring_len0 = logical length before this step's q_len drafts."""
     rng = np.random.default_rng(seed)
@@ -277,4 +297,5 @@ WORKLOADS = {
     "llama70b_mixed": llama70b_mixed,
     "prefix": prefix,
     "ring": ring,
+    "prefill_70b": prefill_70b,
 }
