@@ -52,7 +52,8 @@ from paged_kv_cache_147_gb300 import replicas, workloads  # noqa: E402
 METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak), decode tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
-ALL_WORKLOADS = ["llama70b_b16", "edge_1p1b", "llama70b_mixed", "prefix", "ring"]
+ALL_WORKLOADS = ["llama70b_b16", "edge_1p1b", "llama70b_mixed", "prefix", "ring", "prefill_70b",
+                 "prefix_private"]
 
 
 def parse_args(argv=None):
@@ -63,7 +64,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama70b_b16", choices=ALL_WORKLOADS,
                     help="the headline workload (default: the largest single-GPU one)")
-    ap.add_argument("--also", default="edge_1p1b,llama70b_mixed,prefix,ring",
+    ap.add_argument("--also", default="edge_1p1b,llama70b_mixed,prefix,ring,prefill_70b",
                     help="comma-separated workloads measured after the headline and reported "
                          "under per_workload ('none': headline only)")
     ap.add_argument("--min-seconds", type=float, default=1.5,
@@ -92,9 +93,38 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """Dense f16/bf16 tensor-core peak: the measured cuBLAS bf16 rates (f16 runs at the bf16
+    rate on these tensor cores: nominal ratio 1), burst and sustained."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def prefill_flops(w) -> int:
+    """Algorithmic flops of one chunked-prefill step over all layers: every visible (query,
+    key) pair of every query head costs 2 x 128 for Q K^T and 2 x 128 for P V."""
+    ctx = w.context_lens.astype(np.int64)
+    first = ctx - w.q_len
+    pairs = 0
+    for b in range(w.num_seqs):
+        i = np.arange(w.q_len, dtype=np.int64)
+        pairs += int(np.maximum(0, np.minimum(ctx[b], first[b] + i + 1)).sum())
+    return pairs * w.num_q_heads * w.head_dim * 4 * w.num_layers
+
+
 def make_workload(name, layers=None):
     # the ring cache spans 24 layers of the 1.1B shape, so that a step exceeds L2
-    w = workloads.ring(num_layers=24) if name == "ring" else workloads.WORKLOADS[name]()
+    if name == "ring":
+        w = workloads.ring(num_layers=24)
+    elif name == "prefix_private":
+        w = workloads.prefix(private=True)
+    else:
+        w = workloads.WORKLOADS[name]()
     if layers is not None:
         w.num_layers = max(1, min(layers, w.num_layers))
     return w
@@ -218,7 +248,8 @@ class Step:
         self.dev = dev
         # fused append + decode per layer (paged workloads), copy-on-write then fused (prefix),
         # drafts / rollback / one more token (ring), or the E4M3 form of the fused step
-        self.kind = {"prefix": "prefix", "ring": "ring"}.get(w.name, "fused")
+        self.kind = {"prefix": "prefix", "prefix_private": "prefix",
+                     "ring": "ring"}.get(w.name, "fused")
         if kv == "fp8":
             if self.kind != "fused":
                 raise SystemExit("--kv fp8 applies to the paged GQA workloads")
@@ -592,7 +623,7 @@ def measure_workload(args, w, local_rank, world_size, kv="fp16"):
         roof_graph = capture(st.run_roofline)
         r_med, _, _, _ = time_graph(roof_graph, steps, args.warmup, min_s / 2)
         per_launch = r_med / steps / nroof
-    if w.name == "prefix":
+    if w.name.startswith("prefix"):
         bytes_launch = unique_bytes(w) / w.num_layers
     else:
         bytes_launch = bytes_step / nroof
@@ -640,7 +671,7 @@ def measure_workload(args, w, local_rank, world_size, kv="fp16"):
         "gpu_launches": st.launches_per_step * steps * reps,
         "clocks": clk,
     }
-    if w.name == "prefix":
+    if w.name.startswith("prefix"):
         ub = unique_bytes(w)
         line["unique_kv_bytes_per_step"] = ub
         line["unique_gbs"] = round(ub * steps * world_size / t_max / 1e9, 2)
@@ -651,21 +682,124 @@ def measure_workload(args, w, local_rank, world_size, kv="fp16"):
     return line
 
 
+class PrefillStep:
+    """One chunked-prefill step: per layer the chunk's K/V rows are appended (slot mapping once,
+    then kv_append) and the chunk attends causally over the paged cache (paged_prefill)."""
+
+    def __init__(self, w, dev):
+        from paged_kv_cache_147_gb300 import pkv
+        self.pkv, self.w, self.dev = pkv, w, dev
+        self.k, self.v = w.pools(dev)
+        self.bt = torch.as_tensor(w.block_tables, device=dev)
+        self.cl = torch.as_tensor(w.context_lens, device=dev)
+        seq, pos = w.new_token_positions()
+        self.seq = torch.as_tensor(seq, device=dev)
+        self.pos = torch.as_tensor(pos, device=dev)
+        self.slots = torch.empty(seq.shape[0], dtype=torch.int64, device=dev)
+        self.q = torch.stack([w.query(l, dev) for l in range(w.num_layers)])
+        kv_rows = [w.new_kv(l, dev) for l in range(w.num_layers)]
+        self.kn = torch.stack([a for a, _ in kv_rows])
+        self.vn = torch.stack([b for _, b in kv_rows])
+        self.out = torch.empty_like(self.q)
+        self.in_names = ["q", "kn", "vn", "bt", "cl", "seq", "pos"]
+        self.out_names = ["out"]
+
+    def run(self):
+        p, w = self.pkv, self.w
+        p.slot_mapping(self.seq, self.pos, self.bt, w.block_size, out=self.slots)
+        for l in range(w.num_layers):
+            p.kv_append(self.kn[l], self.vn[l], self.slots, self.k[l], self.v[l])
+            p.paged_prefill(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.cl,
+                            w.scale)
+
+    def run_roofline(self):
+        p, w = self.pkv, self.w
+        for l in range(w.num_layers):
+            p.paged_prefill(self.out[l], self.q[l], self.k[l], self.v[l], self.bt, self.cl,
+                            w.scale)
+
+
+def measure_prefill(args, w, local_rank, world_size):
+    """The chunked-prefill step (NEXT row of the hot path): TFLOP/s of the causal attention
+    over the paged cache, with the prefill kernel's roofline against the tensor-core peak."""
+    dev = f"cuda:{local_rank}"
+    from paged_kv_cache_147_gb300 import pkv
+    st = PrefillStep(w, dev)
+    g = capture(st.run)
+    steps, min_s = args.steps, args.min_seconds
+    clocks = ClockSampler(local_rank)
+    med, reps, _, clk = time_graph(g, steps, args.warmup, min_s, clocks)
+    flops = prefill_flops(w)
+    t_max, total = replicas.aggregate(med, float(flops) * steps, device=dev)
+    value = total / t_max / 1e12
+    rg = capture(st.run_roofline)
+    r_med, _, _, _ = time_graph(rg, steps, args.warmup, min_s / 2)
+    per_launch = r_med / steps / w.num_layers
+    achieved = flops / w.num_layers / per_launch / 1e12
+    burst, sustained, kind = load_tensor_peak()
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(st, g, args, flops, dev, local_rank)
+        for key in ("value", "serial_value"):
+            e2e[key] = round(e2e[key] * 1e9 / 1e12, 2)      # measured as flops / s / 1e9
+        e2e["unit"] = "TFLOP/s"
+    dev_err = pkv.device_error(clear=True)
+    if dev_err:
+        raise RuntimeError(f"device error word {dev_err:#x} after the prefill benchmark")
+    line = {
+        "metric": "chunked-prefill paged attention TFLOP/s (causal, f16 in, f32 accumulate)",
+        "value": round(value, 2), "unit": "TFLOP/s", "steps": steps, "warmup": args.warmup,
+        "repeats": reps, "ms_per_step": round(t_max / steps * 1e3, 4),
+        "dtype": "f16", "config": {
+            "workload": w.name, "layers": w.num_layers, "num_seqs": w.num_seqs,
+            "chunk_q_len": w.q_len, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size,
+            "context_after_chunk": [int(w.context_lens.min()), int(w.context_lens.max())],
+            "flops_per_step": flops,
+            "graph": f"CUDA graph: slot_mapping, {w.num_layers} x (kv_append + paged_prefill)",
+            "timing": f"median of {reps} repeats of {steps} graph replays (>= {min_s:g} s)"},
+        "chunk_tokens_per_s": round(w.num_seqs * w.q_len * steps * world_size / t_max, 1),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": sustained,
+                     "unit": "TFLOP/s", "frac": round(achieved / sustained, 4),
+                     "frac_of_burst_peak": round(achieved / burst, 4), "traffic": None,
+                     "kernel": "prefill_kernel (paged_prefill, tcgen05.mma kind::f16)",
+                     "launch_us": round(per_launch * 1e6, 3),
+                     "algorithmic_flops_per_launch": flops // w.num_layers,
+                     "peak_kind": f"{kind} bf16 dense, sustained (timed inside a seconds-long "
+                                  "loop; f16 = bf16 rate); frac_of_burst_peak against "
+                                  f"{burst:g}"},
+        "e2e": e2e,
+        "gpu_launches": (1 + 2 * w.num_layers) * steps * reps,
+        "clocks": clk,
+    }
+    del st, g, rg
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_ours(args, w, rank, local_rank, world_size):
     torch.cuda.set_device(local_rank)
     from paged_kv_cache_147_gb300 import pkv
     pkv.load()
-    line = measure_workload(args, w, local_rank, world_size, args.kv)
+    if w.name == "prefill_70b":
+        line = measure_prefill(args, w, local_rank, world_size)
+    else:
+        line = measure_workload(args, w, local_rank, world_size, args.kv)
     also = [] if args.also in ("", "none") else [x for x in args.also.split(",") if x]
     per = []
     for name in also:
         if name == w.name or name not in ALL_WORKLOADS:
             continue
-        if args.kv == "fp8" and name in ("prefix", "ring"):
+        if args.kv == "fp8" and name in ("prefix", "ring", "prefill_70b"):
             continue
         gc.collect()
         torch.cuda.empty_cache()
         wx = make_workload(name, args.layers)
+        if name == "prefill_70b":
+            entry = measure_prefill(args, wx, local_rank, world_size)
+            per.append(entry)
+            continue
         entry = measure_workload(args, wx, local_rank, world_size, args.kv)
         for key in ("metric", "n_gpus", "higher_is_better", "scaling", "data", "vs_baseline"):
             entry.pop(key, None)

@@ -220,8 +220,11 @@ def llama70b_mixed(seed: int = 2, num_layers: int = 80) -> Workload:
                     fill, free, ref)
 
 
-def prefix(seed: int = 3) -> Workload:
-    """64 sequences over one shared 4-block prefix; sequences 60..63 are forked children."""
+def prefix(seed: int = 3, private: bool = False) -> Workload:
+    """64 sequences over one shared 4-block prefix; sequences 60..63 are forked children.
+    With ``private`` every sequence gets its own copy of the 4 prefix blocks instead (the same
+    lengths and fork, no cross-sequence sharing of the prefix): the comparison case for what
+    sharing saves in DRAM traffic."""
     rng = np.random.default_rng(seed)
     bs, shared_blocks, n = 64, 4, 64
     suffix = rng.integers(32, 1024, size=n, endpoint=True).astype(np.int32)
@@ -234,10 +237,11 @@ def prefix(seed: int = 3) -> Workload:
     max_blocks = (256 + 1024 + bs - 1) // bs + 1
     # private blocks: sequences 0..59 one set each, 60..63 one set shared
     priv_counts = [(int(lens[b]) - 256 + bs - 1) // bs for b in range(61)]
-    total = shared_blocks + sum(priv_counts) + 8          # 8 spare blocks for copy-on-write
+    n_prefix = shared_blocks * (61 if private else 1)
+    total = n_prefix + sum(priv_counts) + 8               # 8 spare blocks for copy-on-write
     perm = rng.permutation(total).astype(np.int32)
     shared = perm[:shared_blocks]
-    cur = shared_blocks
+    cur = n_prefix
     tables = np.full((n, max_blocks), -1, dtype=np.int32)
     fill = np.zeros(total, dtype=np.int32)
     ref = np.zeros(total, dtype=np.int32)
@@ -249,13 +253,17 @@ def prefix(seed: int = 3) -> Workload:
         for j, blk in enumerate(ids):
             fill[blk] = max(0, min(bs, prior_priv - j * bs))
         owners = [b] if b < 60 else [60, 61, 62, 63]
+        if private:
+            shared = perm[b * shared_blocks:(b + 1) * shared_blocks]
+            fill[shared] = bs
         for o in owners:
             tables[o, :shared_blocks] = shared
             tables[o, shared_blocks:shared_blocks + len(ids)] = ids
             ref[shared] += 1
             ref[ids] += 1
     free = perm[cur:].copy()
-    return Workload("prefix", seed, 1, 32, 32, 128, bs, total, 1, lens, tables, fill, free, ref)
+    return Workload("prefix_private" if private else "prefix", seed, 1, 32, 32, 128, bs, total, 1,
+                    lens, tables, fill, free, ref)
 
 
 def prefill(seed: int, lens, q_len: int, num_q_heads: int, num_kv_heads: int,
