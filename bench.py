@@ -338,17 +338,17 @@ class Step:
                                  for l in range(w.num_layers)])
         self.out_b = torch.empty_like(self.q_b)
         self.rope = pkv.rope_table(w.sink + w.window).to(dev)
-        self.in_names = ["q", "kn", "vn", "bt", "seq", "pos", "L_a", "hw_a", "q_b", "kn_b",
-                         "vn_b", "seq_b", "pos_b", "L_b", "hw_b"]
+        self.in_names = ["q", "kn", "vn", "bt", "L_a", "hw_a", "q_b", "kn_b", "vn_b", "L_b",
+                         "hw_b"]
         self.out_names = ["out", "out_b"]
-        self.launches_per_step = 2 + 4 * w.num_layers
+        self.launches_per_step = 2 * w.num_layers
         self.tokens_per_step = B * (nd + 1)
 
     # -- the step ---------------------------------------------------------------------------------
     def run(self):
         p, w = self.pkv, self.w
         if self.kind == "ring":
-            return self.run_ring(decode=True, append=True)
+            return self.run_ring_fused()
         if self.kind == "prefix":
             # the copies write the pools the fused call reads: it must not start early
             p.copy_blocks(self.k, self.v, self.cow_src, self.cow_dst)
@@ -365,9 +365,23 @@ class Step:
         if self.kind == "prefix":
             p.set_early_start(prev)
 
+    def run_ring_fused(self):
+        """The streaming step, one launch per layer and phase: the drafts through every layer
+        (their rows written to their ring slots and attended causally), the rollback (host
+        state: the second phase's lengths), then one more token through every layer."""
+        p, w = self.pkv, self.w
+        for l in range(w.num_layers):
+            p.ring_attn_decode_append(self.out[l], self.q[l], self.kn[l], self.vn[l], self.k[l],
+                                      self.v[l], self.bt, self.L_a, self.hw_a, w.sink, w.window,
+                                      self.rope, w.scale, self.ws)
+        for l in range(w.num_layers):
+            p.ring_attn_decode_append(self.out_b[l], self.q_b[l], self.kn_b[l], self.vn_b[l],
+                                      self.k[l], self.v[l], self.bt, self.L_b, self.hw_b, w.sink,
+                                      w.window, self.rope, w.scale, self.ws)
+
     def run_ring(self, decode=True, append=True):
-        """The streaming step: the drafts through every layer, the rollback (host state: the
-        second phase's lengths), then one more token through every layer."""
+        """The same step through separate calls (ring slot mapping, kv_append, ring decode),
+        or the decode launches alone."""
         p, w = self.pkv, self.w
         if append:
             p.ring_slot_mapping(self.seq, self.pos, self.bt, w.sink, w.window, w.block_size,
@@ -428,9 +442,9 @@ class Step:
     def graph_note(self) -> str:
         n = self.w.num_layers
         if self.kind == "ring":
-            return (f"CUDA graph: ring_slot_mapping, {n} x (kv_append + ring_attn_decode of "
-                    f"{self.w.q_len} causal drafts); rollback 2; ring_slot_mapping, {n} x "
-                    "(kv_append + ring_attn_decode of 1 token)")
+            return (f"CUDA graph: {n} x ring_attn_decode_append ({self.w.q_len} causal drafts: "
+                    "ring slot mapping + append + decode, one launch); rollback 2; "
+                    f"{n} x ring_attn_decode_append (1 token)")
         if self.kind == "prefix":
             return (f"CUDA graph: copy_blocks (3 copy-on-write copies of the forked children's "
                     f"shared block), {n} x paged_attn_decode_append")
@@ -442,7 +456,8 @@ class Step:
 
     def kernel_note(self) -> str:
         return {"fp8": "decode_kernel, E4M3 cache, fused append (paged_attn_decode_append_fp8)",
-                "ring": "decode_kernel, sink + ring with RoPE on read (ring_attn_decode)"}.get(
+                "ring": "decode_kernel, sink + ring with RoPE on read, fused append "
+                        "(ring_attn_decode_append)"}.get(
             self.kind, "decode_kernel, fused append (paged_attn_decode_append)")
 
 
@@ -617,7 +632,7 @@ def measure_workload(args, w, local_rank, world_size, kv="fp16"):
     # copies, the ring step its slot mappings and appends: there the decode launches are timed
     # alone. The prefix roofline counts the distinct block rows (the shared prefix once).
     nroof = st.roofline_launches()
-    if st.kind in ("fused", "fp8"):
+    if st.kind in ("fused", "fp8", "ring"):
         per_launch = (t_max / steps) / nroof
     else:
         roof_graph = capture(st.run_roofline)
@@ -636,6 +651,13 @@ def measure_workload(args, w, local_rank, world_size, kv="fp16"):
         dg = capture(st.run_decode_only)
         d_med, _, _, _ = time_graph(dg, steps, args.warmup, min_s / 4)
         extra["unfused_decode_launch_us"] = round(d_med / steps / w.num_layers * 1e6, 3)
+    if st.kind == "ring":
+        ug = capture(st.run_ring)
+        u_med, _, _, _ = time_graph(ug, steps, args.warmup, min_s / 4)
+        extra["unfused_step_ms"] = round(u_med / steps * 1e3, 4)
+        dg = capture(lambda: st.run_ring(decode=True, append=False))
+        d_med, _, _, _ = time_graph(dg, steps, args.warmup, min_s / 4)
+        extra["unfused_decode_launch_us"] = round(d_med / steps / nroof * 1e6, 3)
     if st.kind in ("fused", "prefix"):
         ag = capture(st.run_append_only)
         a_med, _, _, _ = time_graph(ag, steps, args.warmup, min_s / 4)

@@ -129,8 +129,8 @@ int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int3
 size_t pkv_decode_workspace_bytes(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
                                   int head_dim);
 
-/* Turns the launch overlap of the fused-append calls (pkv_paged_attn_decode_append and its FP8
- * form) on (enable != 0, the default) or off, for every call made afterwards in this process,
+/* Turns the launch overlap of the fused-append calls (pkv_paged_attn_decode_append, its FP8
+ * form and pkv_ring_attn_decode_append) on (enable != 0, the default) or off, for every call made afterwards in this process,
  * including calls captured into a CUDA graph afterwards. With it off a fused call starts only
  * after the kernel before it has completed, so it may follow a kernel that writes its pools,
  * block tables or context lengths. Returns the previous setting (0 or 1). Not part of the
@@ -252,6 +252,26 @@ int pkv_ring_attn_decode(void* out, const void* q, const void* k_cache, const vo
                          int block_size, int sink, int window, const float* rope_cos_sin,
                          float scale, void* workspace, size_t workspace_bytes,
                          pkv_stream_t stream);
+
+/* Sink + ring decode step with the KV append fused in ([RING] §C 环形 KV 缓存管理内核实现: AppendKV
+ * then attention over FillValidPhysicalIndices' slots, in one launch): for every sequence b and
+ * new token i < q_len at position p = logical_len[b] - q_len + i, its K/V rows k_new, v_new
+ * [(b * q_len + i)][kh][:] are written (before RoPE) to ring slot Slot(p) of pkv_ring_slot_mapping,
+ * exactly as pkv_ring_slot_mapping + pkv_kv_append would, and pkv_ring_attn_decode then runs
+ * over the cache including them. logical_len and high_water are the values after this step's
+ * appends (hw >= L). Requires q_len <= window (the new rows' slots are distinct). Launch overlap
+ * as for pkv_paged_attn_decode_append: before the preceding kernel completes the call reads the
+ * pools, block_tables, logical_len, high_water and rope_cos_sin, so none of them may be written
+ * by the immediately preceding kernel (or call pkv_set_early_start(0)). Other arguments,
+ * workspace and errors as for pkv_ring_attn_decode. */
+int pkv_ring_attn_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                void* k_cache, void* v_cache, int num_blocks,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int64_t* logical_len, const int64_t* high_water,
+                                int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                int head_dim, int block_size, int sink, int window,
+                                const float* rope_cos_sin, float scale, void* workspace,
+                                size_t workspace_bytes, pkv_stream_t stream);
 
 /* ---- FP8 (E4M3) KV cache -------------------------------------------------------------------
  * [VLLM] §工程权衡 (量化与 KV Cache 精度的权衡): FP8 halves the KV cache and is the conservative

@@ -82,6 +82,10 @@ constexpr float kNegInf = -__builtin_huge_valf();
 #define PKV_DECODE_MIN_CTAS 2
 #endif
 constexpr int kMinCtasMt1 = PKV_DECODE_MIN_CTAS;
+// Ring kernels: resident CTAs per SM the register budget is sized for.
+#ifndef PKV_RING_MIN_CTAS
+#define PKV_RING_MIN_CTAS 1
+#endif
 // How long the CTA that merges a split unit waits for the unit's other partials before it
 // falls back to announcing its own (normally they are in within microseconds).
 #ifndef PKV_MERGE_WAIT_NS
@@ -507,6 +511,92 @@ __device__ __forceinline__ void expand_e4m3_tile(uint32_t src, uint32_t dst, int
   }
 }
 
+// Ring: rotate-half RoPE of one chunk's 16 keys by their cache index, in place in the chunk's K
+// tile in shared memory (two 64-column halves at stK and stK + kHalfBytes, 128-byte swizzled),
+// by one warp. Lane (p, q) = (lane % 8, lane / 8) takes the dim pairs (i, i + 64), i in
+// [8 p, 8 p + 8), of keys 4 q .. 4 q + 3. Chunk c holds ring slots 16 c .. 16 c + 15; slot t's
+// cache index is t for a sink, else sink + (t - r_lo) mod window. The factors cos / sin(j theta_i)
+// of a group's first key come from the global table's row j; each next key whose index is one
+// more is rotated on by the step factors cos / sin(theta_i) (the table's row 1, which stays in
+// L1), a key after a jump in the index (the ring's wrap) reloads its row.
+__device__ __forceinline__ void rope_pass(const DecodeArgs& a, uint32_t stK, int c, int r_lo,
+                                          int lane) {
+  const int cap = a.sink + a.window;
+  const int p = lane & 7, q = lane >> 3;
+  float step_c[8], step_s[8];
+  {
+    const float4* row = reinterpret_cast<const float4*>(a.rope) + (cap > 1 ? 32 : 0) + 4 * p;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 v = __ldg(row + u);
+      step_c[2 * u] = v.x; step_s[2 * u] = v.y; step_c[2 * u + 1] = v.z; step_s[2 * u + 1] = v.w;
+    }
+  }
+  float fc[8], fs[8];
+  int jprev = -2;
+#pragma unroll 1
+  for (int kk = 0; kk < 4; ++kk) {
+    const int r = 4 * q + kk;
+    const int t = c * kChunk + r;
+    int j = 0;
+    if (t < a.sink) j = t;
+    else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; j = a.sink + d; }
+    if (j != jprev + 1) {
+      const float4* row = reinterpret_cast<const float4*>(a.rope) + j * 32 + 4 * p;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 v = __ldg(row + u);
+        fc[2 * u] = v.x; fs[2 * u] = v.y; fc[2 * u + 1] = v.z; fs[2 * u + 1] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float c2 = fc[u] * step_c[u] - fs[u] * step_s[u];
+        fs[u] = fs[u] * step_c[u] + fc[u] * step_s[u];
+        fc[u] = c2;
+      }
+    }
+    jprev = j;
+    const uint32_t px = stK + swz128(r, p);                // dims 8 p .. 8 p + 7
+    const uint32_t py = stK + kHalfBytes + swz128(r, p);   // dims 64 + 8 p ..
+    const uint4 xv = ld_shared_v4(px), yv = ld_shared_v4(py);
+    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ys[4] = {yv.x, yv.y, yv.z, yv.w};
+    uint32_t xo[4], yo[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&xs[u]));
+      const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&ys[u]));
+      const float c0 = fc[2 * u], s0 = fs[2 * u], c1 = fc[2 * u + 1], s1 = fs[2 * u + 1];
+      xo[u] = pack_half2(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1);
+      yo[u] = pack_half2(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1);
+    }
+    st_shared_v4(px, make_uint4(xo[0], xo[1], xo[2], xo[3]));
+    st_shared_v4(py, make_uint4(yo[0], yo[1], yo[2], yo[3]));
+  }
+}
+
+// Ring: starts the factor rows rope_pass will load for chunk c (the first key of each lane's
+// 4-key group) towards L1, one chunk ahead of their use (lane (p, q): 64 bytes of row j(16 c +
+// 4 q), the part of the row its dims need).
+__device__ __forceinline__ void rope_prefetch(const DecodeArgs& a, int c, int r_lo, int lane) {
+  const int cap = a.sink + a.window;
+  const int t = c * kChunk + 4 * (lane >> 3);
+  int j = 0;
+  if (t < a.sink) j = t;
+  else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; j = a.sink + d; }
+  prefetch_l1(a.rope + j * 128 + 16 * (lane & 7));
+}
+
+// Ring: logical position held by ring slot t of a sequence whose window part starts at position
+// lo_pos (in slot r_lo), or INT_MAX for a slot past the ring's capacity.
+__device__ __forceinline__ int ring_pos(const DecodeArgs& a, int t, int lo_pos, int r_lo) {
+  if (t < a.sink) return t;
+  if (t >= a.sink + a.window) return 0x7fffffff;
+  int d = t - r_lo;
+  if (d < 0) d += a.window;
+  return lo_pos + d;
+}
+
 // Requests segment kk's queries (and, fused append, its new K/V rows) into query buffer kk & 1,
 // completing on that buffer's full barrier; waits first until the consumers have released the
 // buffer's previous use. One thread.
@@ -538,7 +628,8 @@ __device__ __forceinline__ void issue_queries(const DecodeArgs& a, const CUtenso
 // epilogue (merges each segment's per-warp states, writes outputs and split-unit partials,
 // announces arrivals), so the consumers never stop at a unit boundary.
 template <int NCW, int NST, int MT, bool RING, bool APPEND, bool TR, bool FP8>
-__global__ void __launch_bounds__((NCW + 2) * 32, MT == 1 ? kMinCtasMt1 : 1)
+__global__ void __launch_bounds__((NCW + 2) * 32,
+                                  MT != 1 ? 1 : RING ? PKV_RING_MIN_CTAS : kMinCtasMt1)
 decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
   using L = Smem<NCW, NST, MT, FP8>;
@@ -547,8 +638,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   // takes them in order, so it never waits on a full-barrier phase more than one ahead of the
   // last completed one (all that a parity wait can tell apart).
   static_assert(NST % NCW == 0, "pipeline stages must be a multiple of the consumer warps");
-  static_assert(!(RING && APPEND), "the ring variant appends through its own slot mapping");
-  static_assert(!TR || (MT == 1 && !RING), "the transposed tile is for up to 8 rows, paged");
+  static_assert(!TR || MT == 1, "the transposed tile is for up to 8 rows");
+  static_assert(!(FP8 && RING), "the E4M3 cache is paged only");
   static_assert(!FP8 || TR, "the E4M3 cache is read by the transposed tile only");
   // the queries' buffer stays in use for the whole segment when its fragments are not kept in
   // registers, or when it also holds the segment's new K/V rows
@@ -891,6 +982,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         }
       }
       if (!kHoldQ) {
+        if (RING) fence_proxy_async_smem();   // the queries were rotated in place
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
       }
@@ -911,13 +1003,18 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       for (int jj = ((w - j) % NCW + NCW) % NCW; jj < nchunk; jj += NCW) {
         const int gj = j + jj;
         const int st = gj % NST;
+        if (RING) {
+          if (jj < NCW) rope_prefetch(a, s.c0 + jj, r_lo, lane);   // this warp's first chunk
+          if (jj + NCW < nchunk) rope_prefetch(a, s.c0 + jj + NCW, r_lo, lane);
+        }
         if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
         const uint32_t stK = sbase + st * L::kStage;
         uint32_t stV = stK + 2 * kHalfBytes;
         const int c = s.c0 + jj;
-        const bool full_chunk = (c + 1) * kChunk <= Lc - a.q_len + 1;
+        // ring: always masked (the slots' positions are not monotone in the chunk stream)
+        const bool full_chunk = !RING && (c + 1) * kChunk <= Lc - a.q_len + 1;
         bool patched = false;
-        if (APPEND && (c + 1) * kChunk > Lc - a.q_len) {
+        if (APPEND && (RING || (c + 1) * kChunk > Lc - a.q_len)) {
           const int first_new = Lc - a.q_len;
           const int srow = srow_s[st];
           const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
@@ -947,8 +1044,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             const int which = lane >> 4, ch = lane & 15;   // lanes 0-15: K, 16-31: V
             for (int i = 0; i < a.q_len; ++i) {
               const int pos = first_new + i;
-              if (pos < c * kChunk || pos >= (c + 1) * kChunk || pos < 0) continue;
-              const int tok = pos - c * kChunk;
+              if (pos < 0) continue;
+              // the new token's slot in the chunk stream: its position, or its ring slot
+              const int slot = !RING ? pos
+                             : pos < a.sink ? pos : a.sink + (pos - a.sink) % a.window;
+              if (slot < c * kChunk || slot >= (c + 1) * kChunk) continue;
+              const int tok = slot - c * kChunk;
               const uint4 val = ld_shared_v4(nkv + i * 512 + which * 256 + ch * 16);
               st_shared_v4((which ? stV : stK) + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), val);
               if (srow >= 0) {
@@ -966,6 +1067,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           stV = sbase + L::kScratch + w * 2 * kHalfBytes;
           __syncwarp();
           expand_e4m3_tile(stK + kChunk * kD, stV, lane);
+          __syncwarp();
+        }
+        if (RING) {
+          rope_pass(a, stK, c, r_lo, lane);
           __syncwarp();
         }
         // ---- S^T = K Q^T: K fragments as the A operand (keys g, g + 8), two chains ----
@@ -1005,8 +1110,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         float alpha[2];
         bool rescale = false;
 #pragma unroll
+        // positions of keys g and g + 8 (ring: the positions their slots hold)
+        const int pos0 = RING ? ring_pos(a, c * kChunk + g, lo_pos, r_lo) : c * kChunk + g;
+        const int pos1 = RING ? ring_pos(a, c * kChunk + g + 8, lo_pos, r_lo) : c * kChunk + g + 8;
         for (int e = 0; e < 2; ++e) {
-          const int pos0 = c * kChunk + g, pos1 = pos0 + 8;
           float x0 = (sa[e] + sb2[e]) * score_l2;
           float x1 = (sa[2 + e] + sb2[2 + e]) * score_l2;
           if (!full_chunk) {
@@ -1043,8 +1150,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
         if (!full_chunk) {
           const int t0 = c * kChunk + 2 * t4;
-          vm0 = (t0 < Lc ? 0x0000ffffu : 0u) | (t0 + 1 < Lc ? 0xffff0000u : 0u);
-          vm1 = (t0 + 8 < Lc ? 0x0000ffffu : 0u) | (t0 + 9 < Lc ? 0xffff0000u : 0u);
+          if (RING) {
+            vm0 = (ring_pos(a, t0, lo_pos, r_lo) < Lc ? 0x0000ffffu : 0u) |
+                  (ring_pos(a, t0 + 1, lo_pos, r_lo) < Lc ? 0xffff0000u : 0u);
+            vm1 = (ring_pos(a, t0 + 8, lo_pos, r_lo) < Lc ? 0x0000ffffu : 0u) |
+                  (ring_pos(a, t0 + 9, lo_pos, r_lo) < Lc ? 0xffff0000u : 0u);
+          } else {
+            vm0 = (t0 < Lc ? 0x0000ffffu : 0u) | (t0 + 1 < Lc ? 0xffff0000u : 0u);
+            vm1 = (t0 + 8 < Lc ? 0x0000ffffu : 0u) | (t0 + 9 < Lc ? 0xffff0000u : 0u);
+          }
         }
         // ---- O^T += V^T P^T: V fragments (ldmatrix.trans) as the A operand ----
 #pragma unroll
@@ -1057,13 +1171,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           v0 &= vm0; v1 &= vm1; v2 &= vm0; v3 &= vm1;
           mma_16816(ot[dt], v0, v2, v1, v3, pb0, pb1);
         }
-        if (APPEND && patched) fence_proxy_async_smem();
+        if (RING || (APPEND && patched)) fence_proxy_async_smem();
         if (!FP8) {
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_empty + st * 8);
         }
       }
       if (kHoldQ) {
+        if (RING) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
       }
@@ -1136,17 +1251,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const int gj = j + jj;
         const int st = gj % NST;
         if (RING) {
-          // the RoPE rows of this chunk's 16 keys (512 B each) start towards L1 while the
-          // chunk's tiles land: two lines per lane
-          const int t = (s.c0 + jj) * kChunk + (lane >> 1);
-          int jr = -1;
-          if (t < a.sink) jr = t;
-          else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; jr = a.sink + d; }
-          if (jr >= 0) {
-            const float* row = a.rope + jr * 128 + (lane & 1) * 64;
-            prefetch_l1(row);
-            prefetch_l1(row + 32);
-          }
+          if (jj < NCW) rope_prefetch(a, s.c0 + jj, r_lo, lane);   // this warp's first chunk
+          if (jj + NCW < nchunk) rope_prefetch(a, s.c0 + jj + NCW, r_lo, lane);
         }
         if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
         const uint32_t stK = sbase + st * kStageBytes;
@@ -1155,7 +1261,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 
         // positions of this thread's score columns (tokens nt*8 + 2*t4 + e) and of its K rows
         int pcol[2][2];
-        int jk[2] = {0, 0};
   #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
   #pragma unroll
@@ -1171,11 +1276,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
               pcol[nt][e] = p;
             }
           }
-          if (RING) {
-            const int t = c * kChunk + nt * 8 + g;
-            if (t < a.sink) jk[nt] = t;
-            else if (t < cap) { int d = t - r_lo; if (d < 0) d += a.window; jk[nt] = a.sink + d; }
-          }
         }
         // whole chunk visible to every query row?
         bool full_chunk;
@@ -1187,15 +1287,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         // the stale slots in the landed tile and are written to the pool (the chunk's TMA row
         // plus the token's offset: the slot the table maps that position to). ----
         bool patched = false;
-        if (APPEND && (c + 1) * kChunk > Lc - a.q_len) {
+        if (APPEND && (RING || (c + 1) * kChunk > Lc - a.q_len)) {
           const int first_new = Lc - a.q_len;
           const int srow = srow_s[st];
           const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
           const int which = lane >> 4, ch = lane & 15;   // lanes 0-15: K, 16-31: V
           for (int i = 0; i < a.q_len; ++i) {
             const int pos = first_new + i;
-            if (pos < c * kChunk || pos >= (c + 1) * kChunk || pos < 0) continue;
-            const int tok = pos - c * kChunk;
+            if (pos < 0) continue;
+            // the new token's slot in the chunk stream: its position (paged), or its ring slot
+            // Slot(pos) (sink + ring)
+            const int slot = !RING ? pos
+                           : pos < a.sink ? pos : a.sink + (pos - a.sink) % a.window;
+            if (slot < c * kChunk || slot >= (c + 1) * kChunk) continue;
+            const int tok = slot - c * kChunk;
             const uint4 val = ld_shared_v4(nkv + i * 512 + which * 256 + ch * 16);
             st_shared_v4((which ? stV : stK) + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), val);
             if (srow >= 0) {
@@ -1205,6 +1310,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           }
           __syncwarp();
           patched = true;
+        }
+
+        if (RING) {
+          rope_pass(a, stK, c, r_lo, lane);
+          __syncwarp();
         }
 
         // ---- S = Q K^T ----
@@ -1220,29 +1330,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), kf[nt][2 * sp][0],
                     kf[nt][2 * sp][1], kf[nt][2 * sp + 1][0], kf[nt][2 * sp + 1][1]);
           }
-          if (RING) {
-            // rotate-half RoPE on this thread's key row (token nt*8 + g) by its cache index
-            const float4* tab = reinterpret_cast<const float4*>(a.rope) + jk[nt] * 32;
-  #pragma unroll
-            for (int sp = 0; sp < 4; ++sp)
-  #pragma unroll
-              for (int ri = 0; ri < 2; ++ri) {
-                const int d0 = 16 * sp + 8 * ri + 2 * t4;      // even; partner dims d0 + 64
-                const float4 cs = __ldg(tab + (d0 >> 1));
-                const float2 x = __half22float2(*reinterpret_cast<__half2*>(&kf[nt][sp][ri]));
-                const float2 y = __half22float2(*reinterpret_cast<__half2*>(&kf[nt][sp + 4][ri]));
-                kf[nt][sp][ri] = pack_half2(x.x * cs.x - y.x * cs.y, x.y * cs.z - y.y * cs.w);
-                kf[nt][sp + 4][ri] = pack_half2(y.x * cs.x + x.x * cs.y, y.y * cs.z + x.y * cs.w);
-              }
-          }
         }
-        float sc[MT][2][4], sc2[MT][2][4];
+        // two accumulator chains per m-tile (even / odd k-steps) for one m-tile; two m-tiles
+        // already give two independent chains
+        constexpr bool kDual = MT == 1;
+        float sc[MT][2][4], sc2[kDual ? MT : 1][2][4];
   #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
   #pragma unroll
-            for (int i = 0; i < 4; ++i) sc[mt][nt][i] = sc2[mt][nt][i] = 0.f;
+            for (int i = 0; i < 4; ++i) {
+              sc[mt][nt][i] = 0.f;
+              if (kDual) sc2[kDual ? mt : 0][nt][i] = 0.f;
+            }
   #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
@@ -1255,8 +1356,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             }
   #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
-              mma_16816((s8 & 1) ? sc2[mt][nt] : sc[mt][nt], f[0], f[1], f[2], f[3],
-                        kf[nt][s8][0], kf[nt][s8][1]);
+              mma_16816((kDual && (s8 & 1)) ? sc2[kDual ? mt : 0][nt] : sc[mt][nt], f[0], f[1],
+                        f[2], f[3], kf[nt][s8][0], kf[nt][s8][1]);
           }
 
         // ---- mask, online softmax (exp2 domain) ----
@@ -1272,7 +1373,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             for (int nt = 0; nt < 2; ++nt)
   #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                const float x = (sc[mt][nt][rh * 2 + e] + sc2[mt][nt][rh * 2 + e]) * a.scale_log2;
+                const float x = (kDual ? sc[mt][nt][rh * 2 + e] + sc2[kDual ? mt : 0][nt][rh * 2 + e]
+                                       : sc[mt][nt][rh * 2 + e]) * a.scale_log2;
                 v[nt * 2 + e] = (full_chunk || pcol[nt][e] < lim[mt][rh]) ? x : kNegInf;
               }
             float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
@@ -1334,9 +1436,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             mma_16816(o[mt][2 * np + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
           }
         }
-        // a patched tile was written through the generic proxy; order that before the next
-        // TMA (async proxy) write into this stage
-        if (APPEND && patched) fence_proxy_async_smem();
+        // a patched (or, ring, rotated) tile was written through the generic proxy; order that
+        // before the next TMA (async proxy) write into this stage
+        if (RING || (APPEND && patched)) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + st * 8);
       }
@@ -1457,6 +1559,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 // read) and are bound by the consumers' arithmetic: four consumer warps, eight stages.
 constexpr int kNCW = PKV_DECODE_WARPS, kNST = PKV_DECODE_STAGES;
 constexpr int kNCWRing = 4, kNSTRing = 8;
+// The ring's transposed-tile kernels (up to 8 rows): their per-chunk RoPE pass is a chain of
+// dependent shared-memory and arithmetic steps, so more consumer warps hide more of it.
+#ifndef PKV_RING_TR_WARPS
+#define PKV_RING_TR_WARPS 6
+#endif
+#ifndef PKV_RING_TR_STAGES
+#define PKV_RING_TR_STAGES 12
+#endif
+constexpr int kNCWRingTR = PKV_RING_TR_WARPS, kNSTRingTR = PKV_RING_TR_STAGES;
 // The E4M3 cache: 4 KB stages plus a 4 KB fp16 V tile per consumer warp, within the shared
 // memory of the fp16 kernels (two CTAs per SM). Widening the codes adds to each consumer warp's
 // work, so four consumer warps share the chunks (twelve stages, 48 KB of K/V in flight per CTA).
@@ -1489,8 +1600,8 @@ size_t smem_of(int R, int B, int newkv_bytes) {
 
 template <int MT, bool RING, bool APPEND, bool TR = false, bool FP8 = false>
 Variant variant() {
-  constexpr int NCW = RING ? kNCWRing : FP8 ? kNCWFp8 : kNCW;
-  constexpr int NST = RING ? kNSTRing : FP8 ? kNSTFp8 : kNST;
+  constexpr int NCW = RING ? (TR ? kNCWRingTR : kNCWRing) : FP8 ? kNCWFp8 : kNCW;
+  constexpr int NST = RING ? (TR ? kNSTRingTR : kNSTRing) : FP8 ? kNSTFp8 : kNST;
   return Variant{
       reinterpret_cast<const void*>(&decode_kernel<NCW, NST, MT, RING, APPEND, TR, FP8>), MT,
       RING, (NCW + 2) * 32, &smem_of<NCW, NST, MT, FP8>};
@@ -1573,7 +1684,9 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return PKV_EINVAL;
   const bool append = k_new != nullptr;
-  if (append && (ring || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
+  if (append && (!v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
+  // the new tokens of one call must land in distinct ring slots
+  if (append && ring && q_len > window) return PKV_EINVAL;
   const bool fp8 = k_scale != nullptr;
   if (fp8 && (ring || !v_scale || G * q_len > 8)) return PKV_EINVAL;
   if (ring) {
@@ -1593,15 +1706,19 @@ int launch_decode(bool ring, void* out, const void* q, const void* k_new, const 
 
   const int mt = R <= 16 ? 1 : 2;
   // up to 8 rows per unit (GQA groups of 6-8 at one query token): the transposed tile
-  const bool tr = !ring && R <= 8;
+  const bool tr = R <= 8;
   Variant v = fp8      ? (append ? variant<1, false, true, true, true>()
                                  : variant<1, false, false, true, true>())
-              : ring   ? (mt == 1 ? variant<1, true, false>() : variant<2, true, false>())
+              : ring   ? (append ? (tr ? variant<1, true, true, true>()
+                                         : mt == 1 ? variant<1, true, true>() : variant<2, true, true>())
+                                 : (tr ? variant<1, true, false, true>()
+                                       : mt == 1 ? variant<1, true, false>() : variant<2, true, false>()))
               : append ? (tr ? variant<1, false, true, true>()
                              : mt == 1 ? variant<1, false, true>() : variant<2, false, true>())
                        : (tr ? variant<1, false, false, true>()
                              : mt == 1 ? variant<1, false, false>() : variant<2, false, false>());
-  const size_t smem = v.smem(R, num_seqs, append ? 2 * q_len * 512 : 0);
+  const int newkv_bytes = append ? 2 * q_len * 512 : 0;
+  const size_t smem = v.smem(R, num_seqs, newkv_bytes);
   if (smem > 227 * 1024) return PKV_EINVAL;
   int status = PKV_OK;
   const int grid = grid_size(v, smem, &status);
@@ -1796,6 +1913,22 @@ int pkv_ring_attn_decode(void* out, const void* q, const void* k_cache, const vo
                        max_blocks_per_seq, nullptr, logical_len, high_water, num_seqs, q_len,
                        num_q_heads, num_kv_heads, head_dim, block_size, sink, window,
                        rope_cos_sin, scale, workspace, workspace_bytes, stream);
+}
+
+int pkv_ring_attn_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                void* k_cache, void* v_cache, int num_blocks,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int64_t* logical_len, const int64_t* high_water,
+                                int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                int head_dim, int block_size, int sink, int window,
+                                const float* rope_cos_sin, float scale, void* workspace,
+                                size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_seqs > 0 && (!k_new || !v_new)) return PKV_EINVAL;
+  return launch_decode(true, out, q, num_seqs > 0 ? k_new : nullptr, v_new, k_cache, v_cache,
+                       num_blocks, block_tables, max_blocks_per_seq, nullptr, logical_len,
+                       high_water, num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
+                       block_size, sink, window, rope_cos_sin, scale, workspace, workspace_bytes,
+                       stream);
 }
 
 int pkv_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache,

@@ -29,6 +29,7 @@ SYMBOLS = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_allocate", "pkv_pool_warm",
     "pkv_pool_release", "pkv_pool_fork", "pkv_pool_append", "pkv_pool_stats",
     "pkv_pool_refcount", "pkv_spec_verify", "pkv_set_early_start", "pkv_paged_prefill",
+    "pkv_ring_attn_decode_append",
 )
 
 OK, EINVAL, ERANGE, ENOSPC, ECUDA_BASE = 0, -22, -34, -28, -1000
@@ -101,6 +102,8 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
         "pkv_paged_attn_decode_append_fp8": (i32, [P, P, P, P, P, P, P, P, i32, P, i32, P, i32,
                                                    i32, i32, i32, i32, i32, f32, P, sz, P]),
         "pkv_set_early_start": (i32, [i32]),
+        "pkv_ring_attn_decode_append": (i32, [P, P, P, P, P, P, i32, P, i32, P, P, i32, i32, i32,
+                                              i32, i32, i32, i32, i32, P, f32, P, sz, P]),
         "pkv_paged_prefill": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32, i32, f32,
                                     P]),
         "pkv_pool_create": (i32, [i32, i32, i32, P]),
@@ -318,6 +321,22 @@ def ring_attn_decode(out, q, k_cache, v_cache, block_tables, logical_len, high_w
         _p(out), _p(q), _p(k_cache), _p(v_cache), nb, _p(block_tables), block_tables.shape[1],
         _p(logical_len), _p(high_water), B, q_len, hq, hkv, d, bs, sink, window,
         _p(rope_cos_sin), float(scale), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def ring_attn_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_tables, logical_len,
+                            high_water, sink, window, rope_cos_sin, scale, workspace,
+                            stream=None):
+    """Sink + ring decode step with the append fused in: k_new, v_new [B*q_len, Hkv, D] (before
+    RoPE) go to the ring slots of positions logical_len[b] - q_len + i, then ring attention runs
+    over the cache including them. Early-start caveat as for paged_attn_decode_append."""
+    B, q_len, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    _check("pkv_ring_attn_decode_append", load().pkv_ring_attn_decode_append(
+        _p(out), _p(q), _p(k_new), _p(v_new), _p(k_cache), _p(v_cache), nb, _p(block_tables),
+        block_tables.shape[1], _p(logical_len), _p(high_water), B, q_len, hq, hkv, d, bs, sink,
+        window, _p(rope_cos_sin), float(scale), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 

@@ -187,18 +187,26 @@ def test_prefix_fork_copy_on_write():
     _check_layer(w, 0, k_all, v_all, bt_d, cl_d, slots_d, orc_slots, ws)
 
 
-def _ring_step(w, k_l, v_l, bt_d, rope_d, ws, k_host, v_host, L, hw, q_len, kn, vn, q):
+def _ring_step(w, k_l, v_l, bt_d, rope_d, ws, k_host, v_host, L, hw, q_len, kn, vn, q,
+               fused=False):
+    """Append the step's rows at their ring slots and decode: ring slot mapping + kv_append +
+    ring_attn_decode, or the one fused call; the oracle replays the append on its host copy."""
     seq = np.repeat(np.arange(w.num_seqs, dtype=np.int32), q_len)
     pos = (L[:, None] - q_len + np.arange(q_len)[None, :]).reshape(-1).astype(np.int64)
-    slots_d = pkv.ring_slot_mapping(_dev(seq, torch.int32), _dev(pos, torch.int64), bt_d,
-                                    w.sink, w.window, w.block_size)
     orc_slots = oracle.ring_slot_mapping(seq, pos, w.block_tables, w.sink, w.window, w.block_size)
-    pkv.kv_append(kn, vn, slots_d, k_l, v_l)
     out = torch.empty_like(q)
-    pkv.ring_attn_decode(out, q, k_l, v_l, bt_d, _dev(L, torch.int64), _dev(hw, torch.int64),
-                         w.sink, w.window, rope_d, w.scale, ws)
-    torch.cuda.synchronize()
-    assert np.array_equal(slots_d.cpu().numpy(), orc_slots)
+    if fused:
+        pkv.ring_attn_decode_append(out, q, kn, vn, k_l, v_l, bt_d, _dev(L, torch.int64),
+                                    _dev(hw, torch.int64), w.sink, w.window, rope_d, w.scale, ws)
+        torch.cuda.synchronize()
+    else:
+        slots_d = pkv.ring_slot_mapping(_dev(seq, torch.int32), _dev(pos, torch.int64), bt_d,
+                                        w.sink, w.window, w.block_size)
+        pkv.kv_append(kn, vn, slots_d, k_l, v_l)
+        pkv.ring_attn_decode(out, q, k_l, v_l, bt_d, _dev(L, torch.int64), _dev(hw, torch.int64),
+                             w.sink, w.window, rope_d, w.scale, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(slots_d.cpu().numpy(), orc_slots)
     oracle.kv_append(f16_host(kn), f16_host(vn), orc_slots, k_host, v_host, w.block_size)
     assert np.array_equal(u16(k_l), k_host.view(np.uint16))
     assert np.array_equal(u16(v_l), v_host.view(np.uint16))
@@ -207,7 +215,8 @@ def _ring_step(w, k_l, v_l, bt_d, rope_d, ws, k_host, v_host, L, hw, q_len, kn, 
     return out, ref
 
 
-def test_ring_drafts_rollback_append():
+@pytest.mark.parametrize("fused", [False, True])
+def test_ring_drafts_rollback_append(fused):
     w = workloads.ring()
     k_all, v_all = w.pools(DEV)
     k_l, v_l = k_all[0], v_all[0]
@@ -221,15 +230,68 @@ def test_ring_drafts_rollback_append():
     q = w.query(0, DEV)
     L = L0 + 4
     hw = L.copy()
-    out, ref = _ring_step(w, k_l, v_l, bt_d, rope_d, ws, k_host, v_host, L, hw, 4, kn, vn, q)
+    out, ref = _ring_step(w, k_l, v_l, bt_d, rope_d, ws, k_host, v_host, L, hw, 4, kn, vn, q,
+                          fused)
     assert_attn_close(out, ref, "ring drafts")
     # roll back 2 (high-water mark stays), append one token at L0 + 2, decode it
     L = L0 + 3
     kn1 = w.draw((w.num_seqs, 2, 128), 0, 100, DEV)
     vn1 = w.draw((w.num_seqs, 2, 128), 0, 101, DEV)
     q1 = w.draw((w.num_seqs, 1, 12, 128), 0, 102, DEV)
-    out, ref = _ring_step(w, k_l, v_l, bt_d, rope_d, ws, k_host, v_host, L, hw, 1, kn1, vn1, q1)
+    out, ref = _ring_step(w, k_l, v_l, bt_d, rope_d, ws, k_host, v_host, L, hw, 1, kn1, vn1, q1,
+                          fused)
     assert_attn_close(out, ref, "ring after rollback")
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_ring_drafts_across_the_wrap_and_in_the_sinks(fused):
+    """Drafts whose ring slots wrap from the window's end to its start, drafts that begin
+    inside the sinks of a young sequence, and one ending right at the first wrap."""
+    w = workloads.ring()
+    S, W = w.sink, w.window
+    L0 = w.ring_len0.astype(np.int64).copy()
+    L0[:4] = [S + 10 * W + W - 2, 3, S + W - 1, 1021]
+    k_all, v_all = w.pools(DEV)
+    k_l, v_l = k_all[0], v_all[0]
+    k_host, v_host = f16_host(k_l).copy(), f16_host(v_l).copy()
+    bt_d = _dev(w.block_tables, torch.int32)
+    rope_d = pkv.rope_table(S + W).to(DEV)
+    ws = pkv.make_workspace(w.num_seqs, 4, w.num_q_heads, w.num_kv_heads)
+    kn, vn = w.new_kv(0, DEV)
+    q = w.query(0, DEV)
+    out, ref = _ring_step(w, k_l, v_l, bt_d, rope_d, ws, k_host, v_host, L0 + 4, L0 + 4, 4,
+                          kn, vn, q, fused)
+    assert_attn_close(out, ref, "ring drafts across the wrap")
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_ring_multi_layer_pool_at_layer_stride(fused):
+    """The streaming step on layers 1 and 2 of a 3-layer pool (each layer's base pointer at the
+    layer stride): every layer's bytes, the untouched layer 0 included, and every output."""
+    w = workloads.ring(num_layers=3)
+    k_all, v_all = w.pools(DEV)
+    hosts = [(f16_host(k_all[l]).copy(), f16_host(v_all[l]).copy()) for l in range(3)]
+    bt_d = _dev(w.block_tables, torch.int32)
+    rope_d = pkv.rope_table(w.sink + w.window).to(DEV)
+    ws = pkv.make_workspace(w.num_seqs, 4, w.num_q_heads, w.num_kv_heads)
+    L0 = w.ring_len0.astype(np.int64)
+    for layer in (1, 2):
+        k_host, v_host = hosts[layer]
+        kn, vn = w.new_kv(layer, DEV)
+        q = w.query(layer, DEV)
+        hw = L0 + 4
+        out, ref = _ring_step(w, k_all[layer], v_all[layer], bt_d, rope_d, ws, k_host, v_host,
+                              L0 + 4, hw, 4, kn, vn, q, fused)
+        assert_attn_close(out, ref, f"ring drafts, layer {layer}")
+        kn1 = w.draw((w.num_seqs, 2, 128), layer, 100, DEV)
+        vn1 = w.draw((w.num_seqs, 2, 128), layer, 101, DEV)
+        q1 = w.draw((w.num_seqs, 1, 12, 128), layer, 102, DEV)
+        out, ref = _ring_step(w, k_all[layer], v_all[layer], bt_d, rope_d, ws, k_host, v_host,
+                              L0 + 3, hw, 1, kn1, vn1, q1, fused)
+        assert_attn_close(out, ref, f"ring after rollback, layer {layer}")
+    for layer in range(3):
+        assert np.array_equal(u16(k_all[layer]), hosts[layer][0].view(np.uint16)), layer
+        assert np.array_equal(u16(v_all[layer]), hosts[layer][1].view(np.uint16)), layer
 
 
 # ------------------------------------------------------------------------------ invariants
