@@ -44,23 +44,23 @@ constexpr int kD = 128;
 constexpr int kM = 128;              // rows of a query tile
 constexpr int kKT = 64;              // keys per tile
 constexpr int kNS = 3;               // K/V stages
-constexpr int kThreads = 192;        // producer, MMA, 4 softmax warps
-constexpr uint32_t kTmemCols = 256;  // S0 [0, 64), S1 [64, 128), O [128, 256)
+constexpr int kThreads = 320;        // producer, MMA, 2 x 4 softmax warps
+constexpr uint32_t kTmemCols = 512;  // S of tiles 0, 1: [0, 64), [64, 128); O: [128, 256), [256, 384)
 constexpr float kLazy = 8.0f;        // log2 of the largest factor before the max is raised
 constexpr float kNegInf = -__builtin_huge_valf();
 // A wait gives up after this long (a healthy pipeline waits microseconds).
 constexpr uint64_t kWaitNs = 500ull * 1000 * 1000;
 
 // shared memory (offsets from a 1024-byte aligned base)
-constexpr int kQ = 0;                        // Q lo / hi halves: 128 rows x 128 B each
-constexpr int kStage0 = 2 * 16384;           // stages: K lo, K hi, V lo, V hi (64 rows x 128 B)
+constexpr int kQBytes = 2 * 16384;             // one query tile: lo / hi halves, 128 rows x 128 B
+constexpr int kQ = 0;                          // two query tiles
+constexpr int kStage0 = 2 * kQBytes;           // stages: K lo, K hi, V lo, V hi (64 rows x 128 B)
 constexpr int kStageBytes = 4 * 8192;
-constexpr int kP = kStage0 + kNS * kStageBytes;   // P buffers: 128 rows x 128 B
+constexpr int kP = kStage0 + kNS * kStageBytes;   // P of each query tile: 128 rows x 128 B
 constexpr int kBar = kP + 2 * 16384;
-// barriers: kv_full[kNS], kv_empty[kNS], q_full, s_full[2], s_free[2], p_full[2], p_free[2],
-// o_final
-constexpr int kNumBars = 2 * kNS + 1 + 8 + 1;
-constexpr int kMisc = kBar + kNumBars * 8;   // TMEM base address, abort flag
+// barriers: kv_full[kNS], kv_empty[kNS], q_full, s_full[2], p_full[2], o_final
+constexpr int kNumBars = 2 * kNS + 1 + 4 + 1;
+constexpr int kMisc = kBar + kNumBars * 8;     // TMEM base address, abort flag
 constexpr int kSmemBytes = kMisc + 16 + 1024;
 
 struct PrefillArgs {
@@ -68,7 +68,7 @@ struct PrefillArgs {
   const int32_t* block_tables;
   const int32_t* context_lens;
   unsigned int* err;
-  int num_blocks, max_blocks, num_seqs, q_len, Hq, Hkv, G, TQ, ntiles;
+  int num_blocks, max_blocks, num_seqs, q_len, Hq, Hkv, G, TQ, ntiles, npairs;
   int block_size, bs_shift;   // bs_shift = log2(block_size)
   float scale_log2;
 };
@@ -92,6 +92,14 @@ __device__ __forceinline__ int context_of(const PrefillArgs& a, int b) {
   return ctx;
 }
 
+// Keys query tile t needs: up to its last valid query's position (0 if the tile is past the
+// chunk).
+__device__ __forceinline__ int tile_kend(const PrefillArgs& a, int t, int ctx) {
+  if (t >= a.ntiles) return 0;
+  const int last_q = min(a.q_len, (t + 1) * a.TQ) - 1;
+  return max(0, min(ctx, ctx - a.q_len + last_q + 1));
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmQ, const PrefillArgs a) {
@@ -103,28 +111,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const uint32_t bar_kv_empty = bar_kv_full + kNS * 8;
   const uint32_t bar_q_full = bar_kv_empty + kNS * 8;
   const uint32_t bar_s_full = bar_q_full + 8;
-  const uint32_t bar_s_free = bar_s_full + 16;
-  const uint32_t bar_p_full = bar_s_free + 16;
-  const uint32_t bar_p_free = bar_p_full + 16;
-  const uint32_t bar_o_final = bar_p_free + 16;
+  const uint32_t bar_p_full = bar_s_full + 16;
+  const uint32_t bar_o_final = bar_p_full + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // unit: (b, h) groups in launch order, the longest query tile of a group first
-  const int grp = blockIdx.x / a.ntiles;
-  const int t = a.ntiles - 1 - (blockIdx.x - grp * a.ntiles);
+  // unit: (b, h) groups in launch order, the pair of longest query tiles of a group first;
+  // pair u holds query tiles 2 u and 2 u + 1
+  const int grp = blockIdx.x / a.npairs;
+  const int u = a.npairs - 1 - (blockIdx.x - grp * a.npairs);
   const int h = grp % a.Hkv, b = grp / a.Hkv;
-  const int rows = a.TQ * a.G;              // rows of the tile in use
+  const int rows = a.TQ * a.G;              // rows of a tile in use
   const int raw_ctx = __ldg(a.context_lens + b);
   const int ctx = context_of(a, b);
   if (tid == 0 && raw_ctx != ctx) atomicOr(a.err, PKV_DEVERR_CONTEXT);
   const int first_pos = ctx - a.q_len;      // position of the chunk's first query
-  // keys this tile needs: up to the last valid query's position
-  const int last_q = min(a.q_len, (t + 1) * a.TQ) - 1;
-  const int kend = max(0, min(ctx, first_pos + last_q + 1));
-  const int nkt = (kend + kKT - 1) / kKT;
+  const int t0 = 2 * u;
+  const int kend0 = tile_kend(a, t0, ctx), kend1 = tile_kend(a, t0 + 1, ctx);
+  const int nkt0 = (kend0 + kKT - 1) / kKT, nkt1 = (kend1 + kKT - 1) / kKT;
+  const int kend = max(kend0, kend1);
+  const int nkt = max(nkt0, nkt1);          // key tiles loaded (the later tile needs more)
   const int kpad = (kend + 15) & ~15;       // end of the last 16-token box loaded
+  const bool has1 = t0 + 1 < a.ntiles;
 
   // ---- set-up: barriers, unused query rows zeroed, tensor memory -------------------------------
   if (tid == 0) {
@@ -135,17 +144,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     mbar_init(bar_q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s_full + i * 8, 1);
-      mbar_init(bar_s_free + i * 8, 128);
       mbar_init(bar_p_full + i * 8, 128);
-      mbar_init(bar_p_free + i * 8, 1);
     }
     mbar_init(bar_o_final, 1);
     *abort = 0;
   }
-  // rows the query box does not cover still go through the MMA: make them finite
-  for (int i = rows * 8 + tid; i < kM * 8; i += kThreads) {
-    reinterpret_cast<uint4*>(smem + kQ)[i] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(smem + kQ + 16384)[i] = make_uint4(0, 0, 0, 0);
+  // rows the query boxes do not cover still go through the MMA: make them finite (a missing
+  // second tile is all zeros)
+  for (int ti = 0; ti < 2; ++ti) {
+    const int r0 = (ti == 0 || has1) ? rows : 0;
+    for (int i = r0 * 8 + tid; i < kM * 8; i += kThreads) {
+      reinterpret_cast<uint4*>(smem + kQ + ti * kQBytes)[i] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(smem + kQ + ti * kQBytes + 16384)[i] = make_uint4(0, 0, 0, 0);
+    }
   }
   fence_proxy_async_smem();
   fence_barrier_init();
@@ -161,10 +172,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       prefetch_tensormap(&tmQ);
-      mbar_arrive_expect_tx(bar_q_full, rows * 256);
-      const int qrow = b * a.q_len + t * a.TQ;
-      tma_load_3d(sb0 + kQ, &tmQ, 0, h * a.G, qrow, bar_q_full);
-      tma_load_3d(sb0 + kQ + 16384, &tmQ, 64, h * a.G, qrow, bar_q_full);
+      mbar_arrive_expect_tx(bar_q_full, (has1 ? 2 : 1) * rows * 256);
+      for (int ti = 0; ti < (has1 ? 2 : 1); ++ti) {
+        const int qrow = b * a.q_len + (t0 + ti) * a.TQ;
+        tma_load_3d(sb0 + kQ + ti * kQBytes, &tmQ, 0, h * a.G, qrow, bar_q_full);
+        tma_load_3d(sb0 + kQ + ti * kQBytes + 16384, &tmQ, 64, h * a.G, qrow, bar_q_full);
+      }
     }
     // K/V are read by every query tile of the unit: default L2 policy (they stay for the next)
     int issued = 0;
@@ -172,7 +185,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       if (__shfl_sync(0xffffffffu, *abort, 0)) break;    // one decision for the whole warp
       const int s = j % kNS;
       // block of each of the tile's four 16-token boxes (lane cc < 4); -16: past the keys
-      // this tile needs (an out-of-range box: TMA fills it with zeros)
+      // either query tile needs (an out-of-range box: TMA fills it with zeros)
       int row = -16;
       if (lane < 4) {
         const int tok = j * kKT + lane * 16;
@@ -211,48 +224,67 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __syncwarp();
   } else if (warp == 1) {
     // =================================== MMA issue =============================================
+    // Order: S_0(0), S_1(0); then per key tile j and query tile i: P_i(j) V_j, S_i(j + 1). A
+    // commit tracks every MMA this thread issued before it, so when S_i(j + 1) is done
+    // (s_full_i) P_i(j) V_j is too: the softmax of tile i may then overwrite P_i and rescale
+    // O_i. While one tile's softmax runs, the tensor core works on the other tile.
     if (lane == 0) {
       constexpr uint32_t idS = tc_idesc_f16(kM, kKT, false);
       constexpr uint32_t idO = tc_idesc_f16(kM, kD, true);
+      const int nk[2] = {nkt0, has1 ? nkt1 : 0};
       bool ok = nkt == 0 || mbar_wait_ns(bar_q_full, 0, abort, kWaitNs);
       if (!ok) flag_timeout(a, abort);
-      for (int j = 0; ok && j <= nkt; ++j) {
-        if (j < nkt) {
-          const int s = j % kNS, sb = j & 1;
-          ok = mbar_wait_ns(bar_kv_full + s * 8, (j / kNS) & 1, abort, kWaitNs) &&
-               (j < 2 || mbar_wait_ns(bar_s_free + sb * 8, ((j >> 1) - 1) & 1, abort, kWaitNs));
-          if (!ok) { flag_timeout(a, abort); break; }
-          tc_fence_after();
-          const uint32_t kst = sb0 + kStage0 + s * kStageBytes;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;   // Q lo/hi half
-            const uint32_t koff = (ks >> 2) * 8192 + (ks & 3) * 32;   // K lo/hi half
-            tc_mma_f16(tmem + sb * kKT, tc_desc_sw128(sb0 + kQ + off, 16, 1024),
-                       tc_desc_sw128(kst + koff, 16, 1024), idS, ks > 0);
-          }
-          tc_commit(bar_s_full + sb * 8);
+      int waited = -1;                       // key tiles whose stage is known to have landed
+      auto wait_kv = [&](int j) -> bool {
+        while (waited < j) {
+          const int jj = waited + 1;
+          if (!mbar_wait_ns(bar_kv_full + (jj % kNS) * 8, (jj / kNS) & 1, abort, kWaitNs))
+            return false;
+          waited = jj;
         }
-        if (j >= 1) {
-          const int jp = j - 1, pb = jp & 1, s = jp % kNS;
-          if (!mbar_wait_ns(bar_p_full + pb * 8, (jp >> 1) & 1, abort, kWaitNs)) {
-            ok = false;
-            flag_timeout(a, abort);
-            break;
-          }
+        return true;
+      };
+      auto issue_s = [&](int i, int j) {
+        const uint32_t kst = sb0 + kStage0 + (j % kNS) * kStageBytes;
+        const uint32_t qt = sb0 + kQ + i * kQBytes;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;   // Q lo/hi half
+          const uint32_t koff = (ks >> 2) * 8192 + (ks & 3) * 32;   // K lo/hi half
+          tc_mma_f16(tmem + i * kKT, tc_desc_sw128(qt + off, 16, 1024),
+                     tc_desc_sw128(kst + koff, 16, 1024), idS, ks > 0);
+        }
+        tc_commit(bar_s_full + i * 8);
+      };
+      for (int i = 0; ok && i < 2; ++i) {
+        if (nk[i] == 0) continue;
+        if (!(ok = wait_kv(0))) break;
+        issue_s(i, 0);
+      }
+      for (int j = 0; ok && j < nkt; ++j) {
+        for (int i = 0; i < 2; ++i) {
+          if (j >= nk[i]) continue;
+          if (!(ok = mbar_wait_ns(bar_p_full + i * 8, j & 1, abort, kWaitNs))) break;
           tc_fence_after();
-          const uint32_t vst = sb0 + kStage0 + s * kStageBytes + 16384;
+          const uint32_t vst = sb0 + kStage0 + (j % kNS) * kStageBytes + 16384;
 #pragma unroll
           for (int kt = 0; kt < 4; ++kt) {
             // P: K-major, 16 keys = 32 bytes per step; V: MN-major, 16 keys = two 8-row groups
             // (1024 B apart), the dims' two 64-column halves 8 KB apart
-            tc_mma_f16(tmem + 2 * kKT, tc_desc_sw128(sb0 + kP + pb * 16384 + kt * 32, 16, 1024),
-                       tc_desc_sw128(vst + kt * 2048, 8192, 1024), idO, (jp > 0 || kt > 0));
+            tc_mma_f16(tmem + 2 * kKT + i * kD,
+                       tc_desc_sw128(sb0 + kP + i * 16384 + kt * 32, 16, 1024),
+                       tc_desc_sw128(vst + kt * 2048, 8192, 1024), idO, (j > 0 || kt > 0));
           }
-          tc_commit(bar_kv_empty + s * 8);
-          tc_commit(bar_p_free + pb * 8);
+          if (j + 1 < nk[i]) {
+            if (!(ok = wait_kv(j + 1))) break;
+            issue_s(i, j + 1);
+          }
         }
+        if (!ok) break;
+        tc_commit(bar_kv_empty + (j % kNS) * 8);   // both tiles' P V of key tile j issued
       }
+      if (!ok) flag_timeout(a, abort);
       // every MMA issued (all of them on the normal path) has completed when o_final fires
       tc_commit(bar_o_final);
       if (!mbar_wait_ns(bar_o_final, 0, nullptr, kWaitNs)) flag_timeout(a, abort);
@@ -260,15 +292,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __syncwarp();
   } else {
     // =================================== softmax ===============================================
-    // tcgen05.ld / st are warp-collective (.sync.aligned): every decision that guards them
-    // (the waits, the rescale, the epilogue) is taken for the whole warp.
+    // Warps 2-5 take query tile 0, warps 6-9 tile 1, one thread per row. tcgen05.ld / st are
+    // warp-collective (.sync.aligned): every decision that guards them (the waits, the rescale,
+    // the epilogue) is taken for the whole warp.
+    const int ti = (warp - 2) >> 2;             // query tile of this warp
     const int q4 = warp & 3;                    // TMEM lanes 32 q4 .. 32 q4 + 31
     const int r = 32 * q4 + lane;               // this thread's row
     const int tq = r / a.G, gh = r - tq * a.G;
+    const int t = t0 + ti;
     const int qi = t * a.TQ + tq;
-    const bool valid = r < rows && qi < a.q_len;
+    const bool valid = t < a.ntiles && r < rows && qi < a.q_len;
     const int lim = valid ? max(0, min(ctx, first_pos + qi + 1)) : 0;   // keys t < lim visible
+    const int my_nkt = ti == 0 ? nkt0 : (has1 ? nkt1 : 0);
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    const uint32_t tS = tl + ti * kKT, tO = tl + 2 * kKT + ti * kD;
+    const int ptid = tid - 64 - ti * 128;       // 0 .. 127 within the softmax group
     auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
       const bool w = __all_sync(0xffffffffu, mbar_wait_ns(bar, parity, abort, kWaitNs));
       if (!w && lane == 0) flag_timeout(a, abort);
@@ -276,14 +314,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     };
     float m_used = kNegInf, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkt; ++j) {
-      const int sb = j & 1;
-      if (!(ok = warp_wait(bar_s_full + sb * 8, (j >> 1) & 1))) break;
+    for (int j = 0; j < my_nkt; ++j) {
+      // S_i(j) is done, and with it the P V of tile j - 1 (O is complete up to j - 1, P free)
+      if (!(ok = warp_wait(bar_s_full + ti * 8, j & 1))) break;
       tc_fence_after();
       uint32_t sr[64];
-      tmem_ld64(tl + sb * kKT, sr);
-      tc_fence_before();
-      mbar_arrive(bar_s_free + sb * 8);
+      tmem_ld64(tS, sr);
       float x[64];
       const int base = j * kKT;
       if (base + kKT <= lim) {
@@ -297,24 +333,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       float mx = x[0];
 #pragma unroll
       for (int i = 1; i < 64; ++i) mx = fmaxf(mx, x[i]);
-      // P buffer sb is free once the P V of tile j - 2 is done (which also bounds the state of
-      // the MMA pipeline for the rescale below)
-      if (j >= 2 && !(ok = warp_wait(bar_p_free + sb * 8, ((j >> 1) - 1) & 1))) break;
       const bool raise = mx > m_used + kLazy;
       const bool resc = raise && m_used != kNegInf;   // this row's O and l need rescaling
       if (__any_sync(0xffffffffu, resc)) {
-        // O holds tiles < j: wait for the P V of tile j - 1, then rescale the rows in place
-        // (factor 1 for the warp's other rows)
-        if (!(ok = warp_wait(bar_p_free + (sb ^ 1) * 8, ((j - 1) >> 1) & 1))) break;
+        // rescale the rows in place (factor 1 for the warp's other rows)
         const float f = resc ? fast_exp2(m_used - mx) : 1.f;
-        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
-          tmem_ld32(tl + 2 * kKT + 32 * c, o);
+          tmem_ld32(tO + 32 * c, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tmem_st32(tl + 2 * kKT + 32 * c, o);
+          tmem_st32(tO + 32 * c, o);
         }
         l *= f;
       }
@@ -329,16 +359,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         ph[i] = pack_half2(p0, p1);
       }
       l += rs;
-      // the last box loaded ends at kpad (kend rounded up to 16 tokens); its rows at or past
-      // the context end may hold anything: zero them in V before P V reads them (P is 0
-      // there, but 0 x NaN is not)
+      // the last box loaded ends at kpad; its rows at or past the context end may hold
+      // anything: zero them in V before P V reads them (P is 0 there, but 0 x NaN is not).
+      // Both groups zero the same rows when both use the tile (the same bytes).
       const int s = j % kNS;
       if (j == nkt - 1 && kpad > ctx) {
         if (!(ok = warp_wait(bar_kv_full + s * 8, (j / kNS) & 1))) break;
-        // rows [ctx, kpad) of the tile, in both 64-column halves of V
         const int r0 = ctx - base, r1 = kpad - base;
         const int n = (r1 - r0) * 16;             // 16-byte pieces: rows x (2 halves x 8)
-        for (int i = tid - 64; i < n; i += 128) {
+        for (int i = ptid; i < n; i += 128) {
           const int rr = r0 + i / 16, piece = i % 16;
           const uint32_t addr = sb0 + kStage0 + s * kStageBytes + 16384 + (piece >> 3) * 8192 +
                                 rr * 128 + (piece & 7) * 16;
@@ -346,17 +375,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
       }
       // P row r, 128-byte swizzled (16-byte piece c of row r at (c ^ (r % 8)) * 16)
-      const uint32_t prow = sb0 + kP + sb * 16384 + r * 128;
+      const uint32_t prow = sb0 + kP + ti * 16384 + r * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         st_shared_v4(prow + ((c ^ (r & 7)) << 4),
                      make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]));
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar_p_full + sb * 8);
+      mbar_arrive(bar_p_full + ti * 8);
     }
     // ---- epilogue: O / l, fp16, to the output row ----------------------------------------------
-    const bool have_o = ok && nkt > 0 && warp_wait(bar_o_final, 0);
+    const bool have_o = ok && my_nkt > 0 && warp_wait(bar_o_final, 0);
     const float inv = (have_o && l > 0.f) ? 1.f / l : 0.f;
     __half* dst = a.out + ((static_cast<int64_t>(b) * a.q_len + qi) * a.Hq + h * a.G + gh) * kD;
     if (have_o) tc_fence_after();
@@ -364,7 +393,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
       if (have_o) {
-        tmem_ld32(tl + 2 * kKT + 32 * c, o);    // the whole warp, valid rows or not
+        tmem_ld32(tO + 32 * c, o);              // the whole warp, valid rows or not
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0u;
@@ -429,7 +458,8 @@ extern "C" int pkv_paged_prefill(void* out, const void* q, const void* k_cache,
   // box never exceeds the query tensor)
   const int TQ = std::min(kM / G, q_len);
   const int64_t ntiles = (q_len + TQ - 1) / TQ;
-  const int64_t grid = ntiles * num_kv_heads * num_seqs;
+  const int64_t npairs = (ntiles + 1) / 2;        // two query tiles per CTA
+  const int64_t grid = npairs * num_kv_heads * num_seqs;
   if (rows >= (1ll << 31) || qrows >= (1ll << 31) || grid >= (1ll << 31) ||
       static_cast<int64_t>(max_blocks_per_seq) * block_size >= (1ll << 30))
     return PKV_EINVAL;
@@ -480,6 +510,7 @@ extern "C" int pkv_paged_prefill(void* out, const void* q, const void* k_cache,
   args.G = G;
   args.TQ = TQ;
   args.ntiles = static_cast<int>(ntiles);
+  args.npairs = static_cast<int>(npairs);
   args.block_size = block_size;
   int shift = 0;
   while ((1 << shift) < block_size) ++shift;
