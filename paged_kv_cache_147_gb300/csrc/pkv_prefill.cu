@@ -8,19 +8,24 @@
 // the same operation as paged decode attention with a long query chunk.
 //
 // Design (GB300):
-//  * Work unit = (sequence b, kv head h, query tile): the G query heads of h and TQ = 128 / G
-//    consecutive query tokens form the 128 rows of one M = 128 tile (row = token * G + head),
-//    so every K/V byte a CTA reads serves all G heads. CTAs of one (b, h) are launched next to
-//    each other (the longest tiles first), so their shared K/V stays in L2.
+//  * Query tile = the G query heads of kv head h times TQ = 128 / G consecutive chunk tokens:
+//    the 128 rows of one M = 128 MMA tile (row = token * G + head), so every K/V byte serves all
+//    G heads. A CTA takes two query tiles of one (b, h) and every K/V stage it loads serves
+//    both. CTAs of one (b, h) are launched next to each other (the longest tiles first), so
+//    their shared K/V stays in L2.
 //  * Keys in 64-token tiles: S = Q K^T (M 128, N 64, K 128) into tensor memory, then after the
-//    softmax O += P V (M 128, N 128, K 64), with O accumulated in tensor memory for the whole
-//    context: tcgen05.mma kind::f16, f32 accumulate, issued by one thread.
-//  * Warp roles: warp 0 loads (TMA: the query tile once, then K and V of each key tile as
-//    16-token boxes at the rows the block table gives, into a 3-deep ring of 32 KB stages);
-//    warp 1 allocates tensor memory and issues the MMAs; warps 2-5 run the online softmax, one
-//    thread per row: S from tensor memory, mask, exp2, P (fp16) into shared memory for the
-//    next MMA. S is double-buffered in tensor memory, P in shared memory, so the MMA of key
-//    tile j+1 runs while the softmax of tile j does.
+//    softmax O += P V (M 128, N 128, K 64), with Q and P read from tensor memory (only K and V
+//    come from shared memory, whose bandwidth the MMAs would otherwise saturate) and O
+//    accumulated there for the whole context: tcgen05.mma kind::f16, f32 accumulate, issued
+//    by one thread.
+//  * Warp roles: warp 0 loads (TMA: the query tiles once, then K and V of each key tile as
+//    16-token boxes at the rows the block table gives, into a 4-deep ring of 32 KB stages);
+//    warp 1 allocates tensor memory (512 columns: S, O and Q of each tile) and issues the
+//    MMAs; warps 2-5 and 6-9 copy their query rows into tensor memory, then run the online
+//    softmax of tile 0 and tile 1, one thread per row: S from tensor memory, mask, exp2 (the
+//    score scale folded into its argument), P (fp16) written back over S for the next MMA.
+//    The MMA order alternates the tiles (P_i(j) V_j, then S_i(j + 1)), so the tensor core works
+//    on one tile while the other tile's softmax runs.
 //  * The running maximum is raised only when a row's maximum grows by more than 2^8: the
 //    factor e^(s - m) stays below 256 in fp16 and fp32, and O and the row sum are rescaled
 //    (in tensor memory) only then; the result is the same up to rounding.
@@ -43,9 +48,20 @@ namespace {
 constexpr int kD = 128;
 constexpr int kM = 128;              // rows of a query tile
 constexpr int kKT = 64;              // keys per tile
-constexpr int kNS = 3;               // K/V stages
+#ifndef PKV_PREFILL_STAGES
+#define PKV_PREFILL_STAGES 4
+#endif
+// Key tiles the loader warms L2 with ahead of the one it loads (0: none). A key tile is 16
+// boxes from as many blocks; the first CTA of a (sequence, kv head) to need one misses L2.
+#ifndef PKV_PREFILL_L2_AHEAD
+#define PKV_PREFILL_L2_AHEAD 0
+#endif
+constexpr int kNS = PKV_PREFILL_STAGES;   // K/V stages
+constexpr int kL2Ahead = PKV_PREFILL_L2_AHEAD;
 constexpr int kThreads = 320;        // producer, MMA, 2 x 4 softmax warps
-constexpr uint32_t kTmemCols = 512;  // S of tiles 0, 1: [0, 64), [64, 128); O: [128, 256), [256, 384)
+// S (and P over it) of tile i at 64 i; O of tile i at 128 + 128 i; Q of tile i at 384 + 64 i
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmO = 2 * 64, kTmQ = 2 * 64 + 2 * 128;
 constexpr float kLazy = 8.0f;        // log2 of the largest factor before the max is raised
 constexpr float kNegInf = -__builtin_huge_valf();
 // A wait gives up after this long (a healthy pipeline waits microseconds).
@@ -56,10 +72,9 @@ constexpr int kQBytes = 2 * 16384;             // one query tile: lo / hi halves
 constexpr int kQ = 0;                          // two query tiles
 constexpr int kStage0 = 2 * kQBytes;           // stages: K lo, K hi, V lo, V hi (64 rows x 128 B)
 constexpr int kStageBytes = 4 * 8192;
-constexpr int kP = kStage0 + kNS * kStageBytes;   // P of each query tile: 128 rows x 128 B
-constexpr int kBar = kP + 2 * 16384;
-// barriers: kv_full[kNS], kv_empty[kNS], q_full, s_full[2], p_full[2], o_final
-constexpr int kNumBars = 2 * kNS + 1 + 4 + 1;
+constexpr int kBar = kStage0 + kNS * kStageBytes;
+// barriers: kv_full[kNS], kv_empty[kNS], q_full, q_tmem, s_full[2], p_full[2], o_final
+constexpr int kNumBars = 2 * kNS + 2 + 2 + 2 + 1;
 constexpr int kMisc = kBar + kNumBars * 8;     // TMEM base address, abort flag
 constexpr int kSmemBytes = kMisc + 16 + 1024;
 
@@ -110,8 +125,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const uint32_t bar_kv_full = sb0 + kBar;
   const uint32_t bar_kv_empty = bar_kv_full + kNS * 8;
   const uint32_t bar_q_full = bar_kv_empty + kNS * 8;
-  const uint32_t bar_s_full = bar_q_full + 8;
-  const uint32_t bar_p_full = bar_s_full + 16;
+  const uint32_t bar_q_tmem = bar_q_full + 8;     // the queries are in tensor memory
+  const uint32_t bar_s_full = bar_q_tmem + 8;     // [tile]
+  const uint32_t bar_p_full = bar_s_full + 16;    // [tile]
   const uint32_t bar_o_final = bar_p_full + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kMisc + 4);
@@ -142,6 +158,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       mbar_init(bar_kv_empty + s * 8, 1);
     }
     mbar_init(bar_q_full, 1);
+    mbar_init(bar_q_tmem, 256);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s_full + i * 8, 1);
       mbar_init(bar_p_full + i * 8, 128);
@@ -181,22 +198,33 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
     // K/V are read by every query tile of the unit: default L2 policy (they stay for the next)
     int issued = 0;
+    // TMA row of box cc (< 4) of key tile jt, or -16 past the keys either query tile needs
+    // (an out-of-range box: TMA fills it with zeros); `report` flags a bad block id
+    auto box_row = [&](int jt, int cc, bool report) -> int {
+      const int tok = jt * kKT + cc * 16;
+      if (tok >= kend) return -16;
+      const int blk = __ldg(a.block_tables + static_cast<int64_t>(b) * a.max_blocks +
+                            (tok >> a.bs_shift));
+      if (blk >= 0 && blk < a.num_blocks)
+        return (blk * a.Hkv + h) * a.block_size + (tok & (a.block_size - 1));
+      if (report) atomicOr(a.err, PKV_DEVERR_BLOCK_ID);
+      return -16;
+    };
+    // warm L2 with the first key tiles (lanes: box lane / 4, part lane % 4)
+    if (kL2Ahead > 0 && lane < 16) {
+      for (int jt = 0; jt < min(nkt, kNS + kL2Ahead); ++jt) {
+        const int r = box_row(jt, lane >> 2, false);
+        if (r >= 0) tma_prefetch_l2_2d(((lane & 3) >> 1) ? &tmV : &tmK, (lane & 1) * 64, r);
+      }
+    }
     for (int j = 0; j < nkt; ++j) {
       if (__shfl_sync(0xffffffffu, *abort, 0)) break;    // one decision for the whole warp
       const int s = j % kNS;
-      // block of each of the tile's four 16-token boxes (lane cc < 4); -16: past the keys
-      // either query tile needs (an out-of-range box: TMA fills it with zeros)
-      int row = -16;
-      if (lane < 4) {
-        const int tok = j * kKT + lane * 16;
-        if (tok < kend) {
-          const int blk = __ldg(a.block_tables + static_cast<int64_t>(b) * a.max_blocks +
-                                (tok >> a.bs_shift));
-          if (blk >= 0 && blk < a.num_blocks)
-            row = (blk * a.Hkv + h) * a.block_size + (tok & (a.block_size - 1));
-          else
-            atomicOr(a.err, PKV_DEVERR_BLOCK_ID);
-        }
+      const int row = lane < 4 ? box_row(j, lane, true) : -16;
+      // key tile j + kNS + kL2Ahead towards L2 while tile j's stage is awaited
+      if (kL2Ahead > 0 && lane < 16 && j + kNS + kL2Ahead < nkt) {
+        const int r = box_row(j + kNS + kL2Ahead, lane >> 2, false);
+        if (r >= 0) tma_prefetch_l2_2d(((lane & 3) >> 1) ? &tmV : &tmK, (lane & 1) * 64, r);
       }
       if (lane == 0) {
         if (j >= kNS && !mbar_wait_ns(bar_kv_empty + s * 8, ((j / kNS) - 1) & 1, abort, kWaitNs))
@@ -226,13 +254,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // =================================== MMA issue =============================================
     // Order: S_0(0), S_1(0); then per key tile j and query tile i: P_i(j) V_j, S_i(j + 1). A
     // commit tracks every MMA this thread issued before it, so when S_i(j + 1) is done
-    // (s_full_i) P_i(j) V_j is too: the softmax of tile i may then overwrite P_i and rescale
-    // O_i. While one tile's softmax runs, the tensor core works on the other tile.
+    // (s_full_i) P_i(j) V_j is too: the softmax of tile i may then overwrite P_i (written over
+    // S_i) and rescale O_i. While one tile's softmax runs, the tensor core works on the other.
+    // Q and P come from tensor memory: only K and V are read from shared memory.
     if (lane == 0) {
       constexpr uint32_t idS = tc_idesc_f16(kM, kKT, false);
       constexpr uint32_t idO = tc_idesc_f16(kM, kD, true);
       const int nk[2] = {nkt0, has1 ? nkt1 : 0};
-      bool ok = nkt == 0 || mbar_wait_ns(bar_q_full, 0, abort, kWaitNs);
+      bool ok = nkt == 0 || mbar_wait_ns(bar_q_tmem, 0, abort, kWaitNs);
       if (!ok) flag_timeout(a, abort);
       int waited = -1;                       // key tiles whose stage is known to have landed
       auto wait_kv = [&](int j) -> bool {
@@ -246,14 +275,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       };
       auto issue_s = [&](int i, int j) {
         const uint32_t kst = sb0 + kStage0 + (j % kNS) * kStageBytes;
-        const uint32_t qt = sb0 + kQ + i * kQBytes;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;   // Q lo/hi half
           const uint32_t koff = (ks >> 2) * 8192 + (ks & 3) * 32;   // K lo/hi half
-          tc_mma_f16(tmem + i * kKT, tc_desc_sw128(qt + off, 16, 1024),
-                     tc_desc_sw128(kst + koff, 16, 1024), idS, ks > 0);
+          // Q from tensor memory: 16 dims = 8 columns per step
+          tc_mma_f16_ts(tmem + i * kKT, tmem + kTmQ + i * kKT + ks * 8,
+                        tc_desc_sw128(kst + koff, 16, 1024), idS, ks > 0);
         }
         tc_commit(bar_s_full + i * 8);
       };
@@ -270,11 +298,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           const uint32_t vst = sb0 + kStage0 + (j % kNS) * kStageBytes + 16384;
 #pragma unroll
           for (int kt = 0; kt < 4; ++kt) {
-            // P: K-major, 16 keys = 32 bytes per step; V: MN-major, 16 keys = two 8-row groups
-            // (1024 B apart), the dims' two 64-column halves 8 KB apart
-            tc_mma_f16(tmem + 2 * kKT + i * kD,
-                       tc_desc_sw128(sb0 + kP + i * 16384 + kt * 32, 16, 1024),
-                       tc_desc_sw128(vst + kt * 2048, 8192, 1024), idO, (j > 0 || kt > 0));
+            // P from tensor memory (16 keys = 8 columns per step, over S_i); V: MN-major, 16
+            // keys = two 8-row groups (1024 B apart), the dims' 64-column halves 8 KB apart
+            tc_mma_f16_ts(tmem + kTmO + i * kD, tmem + i * kKT + kt * 8,
+                          tc_desc_sw128(vst + kt * 2048, 8192, 1024), idO, (j > 0 || kt > 0));
           }
           if (j + 1 < nk[i]) {
             if (!(ok = wait_kv(j + 1))) break;
@@ -305,15 +332,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const int lim = valid ? max(0, min(ctx, first_pos + qi + 1)) : 0;   // keys t < lim visible
     const int my_nkt = ti == 0 ? nkt0 : (has1 ? nkt1 : 0);
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-    const uint32_t tS = tl + ti * kKT, tO = tl + 2 * kKT + ti * kD;
+    const uint32_t tO = tl + kTmO + ti * kD;
+    const uint32_t tS = tl + ti * kKT;
     const int ptid = tid - 64 - ti * 128;       // 0 .. 127 within the softmax group
     auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
       const bool w = __all_sync(0xffffffffu, mbar_wait_ns(bar, parity, abort, kWaitNs));
       if (!w && lane == 0) flag_timeout(a, abort);
       return w;
     };
+    const bool sl_pos = a.scale_log2 >= 0.f;
     float m_used = kNegInf, l = 0.f;
     bool ok = true;
+    // this row of the query tile into tensor memory (the A operand of S = Q K^T): 128 dims,
+    // two per column, from the 128-byte-swizzled lo / hi halves in shared memory
+    if (nkt > 0) {                              // the MMA thread waits for all 256 rows
+      ok = warp_wait(bar_q_full, 0);
+      if (ok) {
+        const uint32_t qt = sb0 + kQ + ti * kQBytes;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t qr[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = ld_shared_v4(qt + hf * 16384 + r * 128 + ((c ^ (r & 7)) << 4));
+            qr[4 * c] = v.x; qr[4 * c + 1] = v.y; qr[4 * c + 2] = v.z; qr[4 * c + 3] = v.w;
+          }
+          tmem_st32(tl + kTmQ + ti * kKT + hf * 32, qr);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_q_tmem);
+    }
     for (int j = 0; j < my_nkt; ++j) {
       // S_i(j) is done, and with it the P V of tile j - 1 (O is complete up to j - 1, P free)
       if (!(ok = warp_wait(bar_s_full + ti * 8, j & 1))) break;
@@ -322,17 +371,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       tmem_ld64(tS, sr);
       float x[64];
       const int base = j * kKT;
-      if (base + kKT <= lim) {
+      float mx;
+      const bool unmasked = base + kKT <= lim;
+      if (unmasked) {
+        // the scale is folded into the exponent below: the row's maximum of the raw scores
+        // times the (positive) scale is the maximum of the scaled ones
 #pragma unroll
-        for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(sr[i]) * a.scale_log2;
+        for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(sr[i]);
+        float r0 = x[0];
+#pragma unroll
+        for (int i = 1; i < 64; ++i) r0 = sl_pos ? fmaxf(r0, x[i]) : fminf(r0, x[i]);
+        mx = r0 * a.scale_log2;
       } else {
 #pragma unroll
         for (int i = 0; i < 64; ++i)
           x[i] = base + i < lim ? __uint_as_float(sr[i]) * a.scale_log2 : kNegInf;
-      }
-      float mx = x[0];
+        mx = x[0];
 #pragma unroll
-      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, x[i]);
+        for (int i = 1; i < 64; ++i) mx = fmaxf(mx, x[i]);
+      }
       const bool raise = mx > m_used + kLazy;
       const bool resc = raise && m_used != kNegInf;   // this row's O and l need rescaling
       if (__any_sync(0xffffffffu, resc)) {
@@ -352,11 +409,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       const float m_use = m_used == kNegInf ? 0.f : m_used;
       uint32_t ph[32];
       float rs = 0.f;
+      if (unmasked) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float p0 = fast_exp2(x[2 * i] - m_use), p1 = fast_exp2(x[2 * i + 1] - m_use);
-        rs += p0 + p1;
-        ph[i] = pack_half2(p0, p1);
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = fast_exp2(fmaf(x[2 * i], a.scale_log2, -m_use));
+          const float p1 = fast_exp2(fmaf(x[2 * i + 1], a.scale_log2, -m_use));
+          rs += p0 + p1;
+          ph[i] = pack_half2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = fast_exp2(x[2 * i] - m_use), p1 = fast_exp2(x[2 * i + 1] - m_use);
+          rs += p0 + p1;
+          ph[i] = pack_half2(p0, p1);
+        }
       }
       l += rs;
       // the last box loaded ends at kpad; its rows at or past the context end may hold
@@ -373,14 +440,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                                 rr * 128 + (piece & 7) * 16;
           st_shared_v4(addr, make_uint4(0, 0, 0, 0));
         }
+        fence_proxy_async_smem();
       }
-      // P row r, 128-byte swizzled (16-byte piece c of row r at (c ^ (r % 8)) * 16)
-      const uint32_t prow = sb0 + kP + ti * 16384 + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared_v4(prow + ((c ^ (r & 7)) << 4),
-                     make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]));
-      fence_proxy_async_smem();
+      // P (fp16, two per column) over the first 32 columns of the tile's S, read by P V
+      tmem_st32(tS, ph);
       tc_fence_before();
       mbar_arrive(bar_p_full + ti * 8);
     }
