@@ -53,7 +53,7 @@ METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak), decode tokens/s
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 ALL_WORKLOADS = ["llama70b_b16", "edge_1p1b", "llama70b_mixed", "prefix", "ring", "prefill_70b",
-                 "prefix_private"]
+                 "prefix_private", "spec_verify"]
 
 
 def parse_args(argv=None):
@@ -64,7 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama70b_b16", choices=ALL_WORKLOADS,
                     help="the headline workload (default: the largest single-GPU one)")
-    ap.add_argument("--also", default="edge_1p1b,llama70b_mixed,prefix,ring,prefill_70b",
+    ap.add_argument("--also", default="edge_1p1b,llama70b_mixed,prefix,ring,prefill_70b,"
+                                      "spec_verify",
                     help="comma-separated workloads measured after the headline and reported "
                          "under per_workload ('none': headline only)")
     ap.add_argument("--min-seconds", type=float, default=1.5,
@@ -800,6 +801,44 @@ def measure_prefill(args, w, local_rank, world_size):
     return line
 
 
+def measure_spec_verify(args, local_rank, B=32, K=4, V=32000, seed=6):
+    """Speculative-draft verification beside the ring decode: B sequences, K drafts each, a
+    V-token vocabulary (fp32 logits of the target at K + 1 positions and of the draft at K);
+    GB/s of logits read per call."""
+    from paged_kv_cache_147_gb300 import pkv
+    dev = f"cuda:{local_rank}"
+    g0 = torch.Generator(device=dev)
+    g0.manual_seed(seed)
+    t = torch.randn((B, K + 1, V), generator=g0, device=dev) * 2
+    d = (t[:, :K] + 0.3 * torch.randn((B, K, V), generator=g0, device=dev)).contiguous()
+    x = torch.randint(0, V, (B, K), generator=g0, device=dev, dtype=torch.int32)
+    ua = torch.rand((B, K), generator=g0, device=dev)
+    us = torch.rand(B, generator=g0, device=dev)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    nt = torch.empty_like(n)
+    g = capture(lambda: pkv.spec_verify(t, d, x, ua, us, n, nt))
+    clocks = ClockSampler(local_rank)
+    med, reps, _, clk = time_graph(g, args.steps, args.warmup, args.min_seconds / 2, clocks)
+    per = med / args.steps
+    nbytes = (t.numel() + d.numel()) * 4
+    peak, kind = load_peaks()
+    dev_err = pkv.device_error(clear=True)
+    if dev_err:
+        raise RuntimeError(f"device error word {dev_err:#x} after the spec_verify benchmark")
+    return {"metric": "speculative verify: logits GB/s", "value": round(nbytes / per / 1e9, 2),
+            "unit": "GB/s", "steps": args.steps, "repeats": reps,
+            "us_per_call": round(per * 1e6, 3), "dtype": "f32",
+            "config": {"workload": "spec_verify", "num_seqs": B, "drafts": K, "vocab": V,
+                       "logit_bytes_per_call": nbytes,
+                       "l2": "no flush: the 37 MB of logits fit in L2; reported for the kernel's "
+                             "own speed, not as an HBM measurement"},
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / per / 1e9, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(nbytes / per / 1e9 / peak, 4),
+                         "kernel": "spec_verify_kernel (one cluster of CTAs per sequence)",
+                         "peak_kind": f"{kind} (MEASURED_PEAKS.json hbm_gbs)"},
+            "gpu_launches": args.steps * reps, "clocks": clk}
+
+
 def run_ours(args, w, rank, local_rank, world_size):
     torch.cuda.set_device(local_rank)
     from paged_kv_cache_147_gb300 import pkv
@@ -813,10 +852,13 @@ def run_ours(args, w, rank, local_rank, world_size):
     for name in also:
         if name == w.name or name not in ALL_WORKLOADS:
             continue
-        if args.kv == "fp8" and name in ("prefix", "ring", "prefill_70b"):
+        if args.kv == "fp8" and name in ("prefix", "ring", "prefill_70b", "spec_verify"):
             continue
         gc.collect()
         torch.cuda.empty_cache()
+        if name == "spec_verify":
+            per.append(measure_spec_verify(args, local_rank))
+            continue
         wx = make_workload(name, args.layers)
         if name == "prefill_70b":
             entry = measure_prefill(args, wx, local_rank, world_size)

@@ -328,7 +328,8 @@ int pkv_paged_attn_decode_append_fp8(void* out, const void* q, const void* k_new
  * target_logits float [num_seqs][num_drafts + 1][vocab], draft_logits float
  * [num_seqs][num_drafts][vocab], drafts int32 [num_seqs][num_drafts], u_accept float
  * [num_seqs][num_drafts], u_sample float [num_seqs], outputs int32 [num_seqs]; all device
- * memory. The softmax sums are fp32 block reductions: a decision on a tie within their
+ * memory; num_drafts <= 32. Each sequence is verified by a cluster of up to 8 CTAs that split
+ * the vocabulary. The softmax sums are fp32 reductions: a decision on a tie within their
  * rounding may differ from an exact one. A draft id outside [0, vocab) counts as rejected and
  * sets PKV_DEVERR_TOKEN. */
 int pkv_spec_verify(const float* target_logits, const float* draft_logits, const int32_t* drafts,

@@ -24,12 +24,19 @@ def _softmax64(x):
     return e / e.sum(-1, keepdims=True)
 
 
-@pytest.mark.parametrize("B,K,V,noise", [(32, 4, 32000, 0.3), (64, 4, 151936, 0.1),
-                                          (8, 1, 1000, 1.0), (16, 0, 5000, 0.0)])
-def test_spec_verify_matches_oracle(B, K, V, noise):
+@pytest.mark.parametrize("B,K,V,noise,masked", [(32, 4, 32000, 0.3, 0.0),
+                                                 (64, 4, 151936, 0.1, 0.0),
+                                                 (8, 1, 1000, 1.0, 0.0), (16, 0, 5000, 0.0, 0.0),
+                                                 (16, 3, 40000, 0.3, 0.1), (4, 5, 9000, 0.5, 0.5)])
+def test_spec_verify_matches_oracle(B, K, V, noise, masked):
+    """masked: a fraction of the vocabulary is -inf in both models (banned tokens)."""
     rng = np.random.default_rng(B * 7 + K + V)
     t = (rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32)
     d = (t[:, :K] + noise * rng.standard_normal((B, K, V))).astype(np.float32)
+    if masked > 0:
+        ban = rng.random(V) < masked
+        t[:, :, ban] = -np.inf
+        d[:, :, ban] = -np.inf
     pd = _softmax64(d)
     x = np.zeros((B, K), np.int32)
     for b in range(B):
