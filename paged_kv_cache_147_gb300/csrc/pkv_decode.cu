@@ -129,18 +129,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
 template <int NCW, int NST, int MT, bool FP8 = false>
 struct Smem {
   static constexpr int kNST = NST;
-  // a stage holds one chunk's K and V: fp16 (8 KB) or E4M3 (4 KB: two 16 x 128-byte tiles,
-  // each consumer warp widening its chunks' V tile into a 4 KB fp16 tile of its own)
-  static constexpr int kStage = FP8 ? 2 * kChunk * kD : kStageBytes;
-  static constexpr int kScratch = NST * kStage;        // FP8: NCW x 4 KB fp16 V tiles
+  // a stage holds one chunk's K and V (fp16, 8 KB) or two consecutive chunks' (E4M3, 8 KB: a
+  // 32 x 128-byte K tile, then the V tile, whose codes the consumer warps widen in registers)
+  static constexpr int kChunksPerStage = FP8 ? 2 : 1;
+  static constexpr int kStage = FP8 ? 4 * kChunk * kD : kStageBytes;
   static constexpr int kQHalf = MT * 2048;            // 16*MT rows x 128 B
   static constexpr int kQBuf = 2 * kQHalf;
-  static constexpr int kQ = kScratch + (FP8 ? NCW * 2 * kHalfBytes : 0);
+  static constexpr int kQ = NST * kStage;
   // full[NST], empty[NST], qfull[2], qempty[2], sdone[2], sfree[2]
   static constexpr int kBars = kQ + 2 * kQBuf;
   static constexpr int kFlags = kBars + (2 * NST + 8) * 8;  // abort, pending count + units
-  static constexpr int kSrow = kFlags + 64;             // TMA row of each stage's chunk
-  static constexpr int kState = kSrow + ((NST * 4 + 15) & ~15);
+  static constexpr int kSrow = kFlags + 64;             // TMA row of each stage's chunks
+  static constexpr int kState = kSrow + ((NST * 4 * kChunksPerStage + 15) & ~15);
   // segment states handed from the consumer warps to the epilogue warp, double-buffered:
   // o [2][NCW][R][kSt] (128 used), m [2][NCW][R], l [2][NCW][R]
   __host__ __device__ static int state_floats(int R) { return 2 * NCW * R * (kSt + 2); }
@@ -476,39 +476,17 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
   merge_sync<NT>();                        // stage memory free for the next merge
 }
 
+// Word i (0-3) of a 16-byte vector (i a compile-time constant after unrolling).
+__device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // E4M3 pair (low byte first) -> fp16 pair, exact (every E4M3 value is an fp16 value).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
   uint32_t y;
   asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
       : "=r"(y) : "r"(x));
   return y;
-}
-
-// Widens one chunk's E4M3 V tile (16 rows x 128 bytes, 128B-swizzled as the tensor copy lays it
-// out) into an fp16 tile laid out as an fp16 stage's V is (two 64-column halves of 16 rows x
-// 128 bytes, 128B-swizzled), so that the fp16 transposing fragment loads read it unchanged.
-// One warp: lane-owned 16-byte pieces, 16 codes in, 32 bytes out.
-__device__ __forceinline__ void expand_e4m3_tile(uint32_t src, uint32_t dst, int lane) {
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int item = it * 32 + lane;                 // (row, 16-byte piece)
-    const int r = item >> 3, c8 = item & 7;
-    const uint4 v = ld_shared_v4(src + swz128(r, c8));
-    uint4 lo, hi;
-    lo.x = e4m3x2_to_f16x2(v.x & 0xffffu);
-    lo.y = e4m3x2_to_f16x2(v.x >> 16);
-    lo.z = e4m3x2_to_f16x2(v.y & 0xffffu);
-    lo.w = e4m3x2_to_f16x2(v.y >> 16);
-    hi.x = e4m3x2_to_f16x2(v.z & 0xffffu);
-    hi.y = e4m3x2_to_f16x2(v.z >> 16);
-    hi.z = e4m3x2_to_f16x2(v.w & 0xffffu);
-    hi.w = e4m3x2_to_f16x2(v.w >> 16);
-    // codes 16 c8 .. 16 c8 + 15 are fp16 columns in half c8 / 4, pieces 2 c8 % 8 and + 1
-    const uint32_t base = dst + (c8 >> 2) * kHalfBytes;
-    const int cc = (2 * c8) & 7;
-    st_shared_v4(base + swz128(r, cc), lo);
-    st_shared_v4(base + swz128(r, cc + 1), hi);
-  }
 }
 
 // Ring: rotate-half RoPE of one chunk's 16 keys by their cache index, in place in the chunk's K
@@ -800,19 +778,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             atomicOr(a.err, PKV_DEVERR_BLOCK_ID);
         }
         const int n = min(32, s.c1 - cb);
-        for (int l = 0; l < n; ++l, ++j) {
+        // E4M3: a stage takes chunks l and l + 1 of this group (l + 1 past the segment's end is
+        // an out-of-range row: an all-zero box)
+        for (int l = 0; l < n; l += L::kChunksPerStage, ++j) {
           if (early_kv && !waited && j == NST) {
             // every stage is requested; none frees before the dependency is met
             griddep_wait();
             waited = true;
           }
           const int r = __shfl_sync(0xffffffffu, row, l);
+          const int r2 = FP8 ? __shfl_sync(0xffffffffu, row, (l + 1) & 31) : 0;
           const int st = j % NST;
           const uint32_t fb = bar_full + st * 8;
           if (lane == 0) {
             if (j >= NST && !mbar_wait(bar_empty + st * 8, ((j / NST) - 1) & 1, abort))
               flag_timeout(a, abort);
-            if (APPEND) srow_s[st] = r;   // published to the consumer by the barrier below
+            // published to the consumer by the barrier below
+            if (APPEND) {
+              srow_s[L::kChunksPerStage * st] = r;
+              if (FP8) srow_s[2 * st + 1] = r2;
+            }
             mbar_arrive_expect_tx(fb, L::kStage);
           }
           __syncwarp();                   // the stage is free before any lane writes it
@@ -822,10 +807,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           // once per step: first to go from L2, which then keeps the partials, queries and
           // tables the merges and other CTAs need.
           if (FP8) {
-            // E4M3: one 2 KB box (16 rows x 128 bytes) each for K and V
-            if (lane < 2)
-              tma_load_2d_hint(sbase + st * L::kStage + lane * (kChunk * kD), lane ? &tmV : &tmK,
-                               0, r, fb, kv_policy);
+            // E4M3: 2 KB boxes (16 rows x 128 bytes): K of both chunks, then V of both
+            if (lane < 4)
+              tma_load_2d_hint(sbase + st * L::kStage + lane * (kChunk * kD),
+                               (lane >> 1) ? &tmV : &tmK, 0, (lane & 1) ? r2 : r, fb, kv_policy);
           } else if (lane < 4) {
             tma_load_2d_hint(sbase + st * kStageBytes + lane * kHalfBytes, lane < 2 ? &tmK : &tmV,
                              (lane & 1) * 64, r, fb, kv_policy);
@@ -1000,47 +985,193 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       const float score_l2 = FP8 ? a.scale_log2 * __ldg(a.k_scale + s.h) : a.scale_log2;
       const float out_sc = FP8 ? __ldg(a.v_scale + s.h) : 1.f;
       const int nchunk = s.c1 - s.c0;
-      for (int jj = ((w - j) % NCW + NCW) % NCW; jj < nchunk; jj += NCW) {
-        const int gj = j + jj;
-        const int st = gj % NST;
-        if (RING) {
-          if (jj < NCW) rope_prefetch(a, s.c0 + jj, r_lo, lane);   // this warp's first chunk
-          if (jj + NCW < nchunk) rope_prefetch(a, s.c0 + jj + NCW, r_lo, lane);
-        }
-        if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
-        const uint32_t stK = sbase + st * L::kStage;
-        uint32_t stV = stK + 2 * kHalfBytes;
-        const int c = s.c0 + jj;
-        // ring: always masked (the slots' positions are not monotone in the chunk stream)
-        const bool full_chunk = !RING && (c + 1) * kChunk <= Lc - a.q_len + 1;
-        bool patched = false;
-        if (APPEND && (RING || (c + 1) * kChunk > Lc - a.q_len)) {
-          const int first_new = Lc - a.q_len;
-          const int srow = srow_s[st];
-          const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
-          if constexpr (FP8) {
-            // E4M3 cache: lanes 0-7 quantise a 16-element piece of the new K row, 8-15 of the
-            // V row (divided by the head's scale in binary32, as pkv_kv_append_fp8 does), into
-            // the stage's code tiles and the pool
+      if constexpr (FP8) {
+        // ---- E4M3: a stage holds chunks c and c + 1 of the segment (c + 1 an all-zero box
+        // past its end when the segment has an odd number of chunks). A warp takes whole
+        // stages: 32 keys per online-softmax step, two independent mma chains per product.
+        const int npair = (nchunk + 1) >> 1;
+        for (int jp = ((w - j) % NCW + NCW) % NCW; jp < npair; jp += NCW) {
+          const int gj = j + jp;
+          const int st = gj % NST;
+          if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
+          const uint32_t stK = sbase + st * L::kStage;   // rows 0-15: chunk c, 16-31: c + 1
+          const uint32_t stVc = stK + 2 * kChunk * kD;
+          const int c = s.c0 + 2 * jp;
+          const bool two = c + 1 < s.c1;
+          const int nk = two ? 2 * kChunk : kChunk;      // keys of the segment in the stage
+          const bool full = two && (c + 2) * kChunk <= Lc - a.q_len + 1;
+          bool patched = false;
+          if (APPEND && (c * kChunk + nk > Lc - a.q_len)) {
+            // lanes 0-7 quantise a 16-element piece of a new K row, 8-15 of the V row (divided
+            // by the head's scale in binary32, as pkv_kv_append_fp8 does), into the stage's
+            // code tiles and the pool
+            const int first_new = Lc - a.q_len;
+            const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
             const int which = (lane >> 3) & 1, p = lane & 7;
             const float sc = __ldg((which ? a.v_scale : a.k_scale) + s.h);
             for (int i = 0; i < a.q_len; ++i) {
               const int pos = first_new + i;
-              if (lane >= 16 || pos < c * kChunk || pos >= (c + 1) * kChunk || pos < 0) continue;
-              const int tok = pos - c * kChunk;
+              const int tk = pos - c * kChunk;   // row in the stage's 32-row tiles
+              if (lane >= 16 || pos < 0 || tk < 0 || tk >= nk) continue;
               const uint4 h0 = ld_shared_v4(nkv + i * 512 + which * 256 + p * 32);
               const uint4 h1 = ld_shared_v4(nkv + i * 512 + which * 256 + p * 32 + 16);
               const uint4 q8 = make_uint4(f16x4_to_e4m3x4(h0.x, h0.y, sc),
                                           f16x4_to_e4m3x4(h0.z, h0.w, sc),
                                           f16x4_to_e4m3x4(h1.x, h1.y, sc),
                                           f16x4_to_e4m3x4(h1.z, h1.w, sc));
-              st_shared_v4(stK + which * (kChunk * kD) + swz128(tok, p), q8);
+              st_shared_v4(stK + which * (2 * kChunk * kD) + swz128(tk, p), q8);
+              const int srow = srow_s[2 * st + (tk >> 4)];
               if (srow >= 0) {
                 uint8_t* pool = reinterpret_cast<uint8_t*>(which ? a.v_pool : a.k_pool);
-                *reinterpret_cast<uint4*>(pool + (static_cast<int64_t>(srow) + tok) * kD + p * 16) = q8;
+                *reinterpret_cast<uint4*>(pool + (static_cast<int64_t>(srow) + (tk & 15)) * kD +
+                                          p * 16) = q8;
               }
             }
-          } else {
+            __syncwarp();
+            patched = true;
+          }
+          // ---- S^T = K Q^T for both chunks: keys g and g + 8 of each, one word of four codes
+          // per 16-dim step, widened in registers; two chains per chunk ----
+          float sa[2][4], sb[2][4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sa[h][i] = sb[h][i] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t w0 = ld_shared_u32(stK + swz128(16 * h + g, ks) + 4 * t4);
+              const uint32_t w1 = ld_shared_u32(stK + swz128(16 * h + g + 8, ks) + 4 * t4);
+              const uint32_t a0 = e4m3x2_to_f16x2(w0), a2 = e4m3x2_to_f16x2(w0 >> 16);
+              const uint32_t a1 = e4m3x2_to_f16x2(w1), a3 = e4m3x2_to_f16x2(w1 >> 16);
+              if (ks & 1)
+                mma_16816(sb[h], a0, a1, a2, a3, qb0[ks], qb1[ks]);
+              else
+                mma_16816(sa[h], a0, a1, a2, a3, qb0[ks], qb1[ks]);
+            }
+          }
+          // V codes: dims 16 g .. 16 g + 15 of keys 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9 of each
+          // chunk (the output dims of rows g and g + 8 of the PV tiles below)
+          uint4 vr[2][4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              vr[h][i] = ld_shared_v4(stVc + swz128(16 * h + 2 * t4 + (i & 1) + 8 * (i >> 1), g));
+          if (APPEND && patched) fence_proxy_async_smem();
+          __syncwarp();                      // every code of the stage has been read
+          if (lane == 0) mbar_arrive(bar_empty + st * 8);
+
+          // ---- mask, online softmax over this thread's rows and 4 keys (exp2 domain) ----
+          float pv[2][4], alpha[2];
+          bool rescale = false;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float x[2][2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              x[h][0] = (sa[h][e] + sb[h][e]) * score_l2;           // key g of chunk c + h
+              x[h][1] = (sa[h][2 + e] + sb[h][2 + e]) * score_l2;   // key g + 8
+              if (!full) {
+                const int p0 = (c + h) * kChunk + g;
+                const bool ok = h == 0 || two;
+                x[h][0] = ok && p0 < tlim[e] ? x[h][0] : kNegInf;
+                x[h][1] = ok && p0 + 8 < tlim[e] ? x[h][1] : kNegInf;
+              }
+            }
+            float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_old = tm[e];
+            const float m_new = fmaxf(m_old, mx);
+            const float m_use = m_new == kNegInf ? 0.f : m_new;
+            alpha[e] = fast_exp2(m_old - m_use);
+            rescale |= (m_old != kNegInf) && (m_new != m_old);
+            tm[e] = m_new;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              pv[h][e] = fast_exp2(x[h][0] - m_use);
+              pv[h][2 + e] = fast_exp2(x[h][1] - m_use);
+            }
+            tl[e] = tl[e] * alpha[e] + ((pv[0][e] + pv[0][2 + e]) + (pv[1][e] + pv[1][2 + e]));
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+              ot[dt][0] *= alpha[0];
+              ot[dt][1] *= alpha[1];
+              ot[dt][2] *= alpha[0];
+              ot[dt][3] *= alpha[1];
+            }
+          }
+          // P^T of each chunk (keys x rows) to the B operand: transpose the two 8x8 halves
+          uint32_t pb[2][2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            pb[h][0] = movmatrix_trans(pack_half2(pv[h][0], pv[h][1]));
+            pb[h][1] = movmatrix_trans(pack_half2(pv[h][2], pv[h][3]));
+          }
+          // tokens no query may see may hold anything, NaN included: zero their V entries
+          uint32_t vm[2][2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            vm[h][0] = vm[h][1] = 0xffffffffu;
+            if (!full) {
+              const int t0 = (c + h) * kChunk + 2 * t4;
+              const int lim = (h == 0 || two) ? Lc : 0;
+              vm[h][0] = (t0 < lim ? 0x0000ffffu : 0u) | (t0 + 1 < lim ? 0xffff0000u : 0u);
+              vm[h][1] = (t0 + 8 < lim ? 0x0000ffffu : 0u) | (t0 + 9 < lim ? 0xffff0000u : 0u);
+            }
+          }
+          // ---- O^T += V^T P^T. Row g of tile dt is output dim 16 g + dt, row g + 8 dim
+          // 16 g + 8 + dt (a relabelling of the output dims, undone at the hand-off), so a
+          // thread's A operands are bytes of its own 16-code pieces: byte permutes pair the two
+          // keys of each operand half (low byte: the even key), which widen exactly to fp16 ----
+#pragma unroll
+          for (int dp = 0; dp < 4; ++dp) {
+            const uint32_t sel = (dp & 1) ? 0x7362u : 0x5140u;   // dims 2 dp, 2 dp + 1
+            const int wi = dp >> 1;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t lo01 = __byte_perm(u4_word(vr[h][0], wi), u4_word(vr[h][1], wi), sel);
+              const uint32_t hi01 =
+                  __byte_perm(u4_word(vr[h][0], wi + 2), u4_word(vr[h][1], wi + 2), sel);
+              const uint32_t lo89 = __byte_perm(u4_word(vr[h][2], wi), u4_word(vr[h][3], wi), sel);
+              const uint32_t hi89 =
+                  __byte_perm(u4_word(vr[h][2], wi + 2), u4_word(vr[h][3], wi + 2), sel);
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int sh = 16 * e;
+                const uint32_t a0 = e4m3x2_to_f16x2(lo01 >> sh) & vm[h][0];
+                const uint32_t a1 = e4m3x2_to_f16x2(hi01 >> sh) & vm[h][0];
+                const uint32_t a2 = e4m3x2_to_f16x2(lo89 >> sh) & vm[h][1];
+                const uint32_t a3 = e4m3x2_to_f16x2(hi89 >> sh) & vm[h][1];
+                mma_16816(ot[2 * dp + e], a0, a1, a2, a3, pb[h][0], pb[h][1]);
+              }
+            }
+          }
+        }
+      } else {
+        for (int jj = ((w - j) % NCW + NCW) % NCW; jj < nchunk; jj += NCW) {
+          const int gj = j + jj;
+          const int st = gj % NST;
+          if (RING) {
+            if (jj < NCW) rope_prefetch(a, s.c0 + jj, r_lo, lane);   // this warp's first chunk
+            if (jj + NCW < nchunk) rope_prefetch(a, s.c0 + jj + NCW, r_lo, lane);
+          }
+          if (!mbar_wait(bar_full + st * 8, (gj / NST) & 1, abort)) flag_timeout(a, abort);
+          const uint32_t stK = sbase + st * L::kStage;
+          const uint32_t stV = stK + 2 * kHalfBytes;
+          const int c = s.c0 + jj;
+          // ring: always masked (the slots' positions are not monotone in the chunk stream)
+          const bool full_chunk = !RING && (c + 1) * kChunk <= Lc - a.q_len + 1;
+          bool patched = false;
+          if (APPEND && (RING || (c + 1) * kChunk > Lc - a.q_len)) {
+            const int first_new = Lc - a.q_len;
+            const int srow = srow_s[st];
+            const uint32_t nkv = sbase + L::newkv_off(a.R, B) + qs * a.q_len * 512;
             const int which = lane >> 4, ch = lane & 15;   // lanes 0-15: K, 16-31: V
             for (int i = 0; i < a.q_len; ++i) {
               const int pos = first_new + i;
@@ -1057,122 +1188,95 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 *reinterpret_cast<uint4*>(pool + (static_cast<int64_t>(srow) + tok) * kD + ch * 8) = val;
               }
             }
+            __syncwarp();
+            patched = true;
           }
-          __syncwarp();
-          patched = true;
-        }
-        if constexpr (FP8) {
-          // widen the V codes into this warp's fp16 tile (its previous chunk's reads are
-          // done); the K codes are read in place below
-          stV = sbase + L::kScratch + w * 2 * kHalfBytes;
-          __syncwarp();
-          expand_e4m3_tile(stK + kChunk * kD, stV, lane);
-          __syncwarp();
-        }
-        if (RING) {
-          rope_pass(a, stK, c, r_lo, lane);
-          __syncwarp();
-        }
-        // ---- S^T = K Q^T: K fragments as the A operand (keys g, g + 8), two chains ----
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
-        if constexpr (FP8) {
-          // keys g and g + 8: one word of four codes each per 16-dim step, widened in registers
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t w0 = ld_shared_u32(stK + swz128(g, ks) + 4 * t4);
-            const uint32_t w1 = ld_shared_u32(stK + swz128(g + 8, ks) + 4 * t4);
-            const uint32_t a0 = e4m3x2_to_f16x2(w0 & 0xffffu), a2 = e4m3x2_to_f16x2(w0 >> 16);
-            const uint32_t a1 = e4m3x2_to_f16x2(w1 & 0xffffu), a3 = e4m3x2_to_f16x2(w1 >> 16);
-            if (ks & 1)
-              mma_16816(sb2, a0, a1, a2, a3, qb0[ks], qb1[ks]);
-            else
-              mma_16816(sa, a0, a1, a2, a3, qb0[ks], qb1[ks]);
-          }
-          if (APPEND && patched) fence_proxy_async_smem();
-          __syncwarp();                      // every code of the stage has been read
-          if (lane == 0) mbar_arrive(bar_empty + st * 8);
-        }
-#pragma unroll
-        for (int sp = 0; sp < (FP8 ? 0 : 4); ++sp) {
-          uint32_t k0[4], k1[4];   // keys 0-7 and 8-15, dims 32 sp .. 32 sp + 31
-          const int ch = 4 * sp + (lane >> 3);
-          ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(lane & 7, ch & 7), k0[0], k0[1], k0[2],
-                  k0[3]);
-          ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(8 + (lane & 7), ch & 7), k1[0], k1[1],
-                  k1[2], k1[3]);
-          // k-step 2 sp (dims 32 sp .. +15) and 2 sp + 1 (dims 32 sp + 16 .. +31)
-          mma_16816(sa, k0[0], k1[0], k0[1], k1[1], qb0[2 * sp], qb1[2 * sp]);
-          mma_16816(sb2, k0[2], k1[2], k0[3], k1[3], qb0[2 * sp + 1], qb1[2 * sp + 1]);
-        }
-        // ---- mask, online softmax over this thread's rows (exp2 domain) ----
-        // sa: [0] key g row 2t4, [1] key g row 2t4+1, [2] key g+8 row 2t4, [3] key g+8 row 2t4+1
-        float pv[4];
-        float alpha[2];
-        bool rescale = false;
-#pragma unroll
-        // positions of keys g and g + 8 (ring: the positions their slots hold)
-        const int pos0 = RING ? ring_pos(a, c * kChunk + g, lo_pos, r_lo) : c * kChunk + g;
-        const int pos1 = RING ? ring_pos(a, c * kChunk + g + 8, lo_pos, r_lo) : c * kChunk + g + 8;
-        for (int e = 0; e < 2; ++e) {
-          float x0 = (sa[e] + sb2[e]) * score_l2;
-          float x1 = (sa[2 + e] + sb2[2 + e]) * score_l2;
-          if (!full_chunk) {
-            x0 = pos0 < tlim[e] ? x0 : kNegInf;
-            x1 = pos1 < tlim[e] ? x1 : kNegInf;
-          }
-          float mx = fmaxf(x0, x1);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float m_old = tm[e];
-          const float m_new = fmaxf(m_old, mx);
-          const float m_use = m_new == kNegInf ? 0.f : m_new;
-          alpha[e] = fast_exp2(m_old - m_use);
-          rescale |= (m_old != kNegInf) && (m_new != m_old);
-          tm[e] = m_new;
-          pv[e] = fast_exp2(x0 - m_use);
-          pv[2 + e] = fast_exp2(x1 - m_use);
-          tl[e] = tl[e] * alpha[e] + (pv[e] + pv[2 + e]);
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-          for (int dt = 0; dt < 8; ++dt) {
-            ot[dt][0] *= alpha[0];
-            ot[dt][1] *= alpha[1];
-            ot[dt][2] *= alpha[0];
-            ot[dt][3] *= alpha[1];
-          }
-        }
-        // P^T (keys x rows) to the B operand (rows g, keys 2t4..): transpose the two 8x8 halves
-        const uint32_t pb0 = movmatrix_trans(pack_half2(pv[0], pv[1]));
-        const uint32_t pb1 = movmatrix_trans(pack_half2(pv[2], pv[3]));
-        // tokens no query may see may hold anything, NaN included: zero their V entries
-        uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-        if (!full_chunk) {
-          const int t0 = c * kChunk + 2 * t4;
           if (RING) {
-            vm0 = (ring_pos(a, t0, lo_pos, r_lo) < Lc ? 0x0000ffffu : 0u) |
-                  (ring_pos(a, t0 + 1, lo_pos, r_lo) < Lc ? 0xffff0000u : 0u);
-            vm1 = (ring_pos(a, t0 + 8, lo_pos, r_lo) < Lc ? 0x0000ffffu : 0u) |
-                  (ring_pos(a, t0 + 9, lo_pos, r_lo) < Lc ? 0xffff0000u : 0u);
-          } else {
-            vm0 = (t0 < Lc ? 0x0000ffffu : 0u) | (t0 + 1 < Lc ? 0xffff0000u : 0u);
-            vm1 = (t0 + 8 < Lc ? 0x0000ffffu : 0u) | (t0 + 9 < Lc ? 0xffff0000u : 0u);
+            rope_pass(a, stK, c, r_lo, lane);
+            __syncwarp();
           }
-        }
-        // ---- O^T += V^T P^T: V fragments (ldmatrix.trans) as the A operand ----
-#pragma unroll
-        for (int dt = 0; dt < 8; ++dt) {
-          const int i = lane >> 3;
-          const int tok = (i & 1) * 8 + (lane & 7);
-          const int ch = 2 * dt + (i >> 1);
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_trans(stV + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), v0, v1, v2, v3);
-          v0 &= vm0; v1 &= vm1; v2 &= vm0; v3 &= vm1;
-          mma_16816(ot[dt], v0, v2, v1, v3, pb0, pb1);
-        }
-        if (RING || (APPEND && patched)) fence_proxy_async_smem();
-        if (!FP8) {
+          // ---- S^T = K Q^T: K fragments as the A operand (keys g, g + 8), two chains ----
+          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+          for (int sp = 0; sp < 4; ++sp) {
+            uint32_t k0[4], k1[4];   // keys 0-7 and 8-15, dims 32 sp .. 32 sp + 31
+            const int ch = 4 * sp + (lane >> 3);
+            ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(lane & 7, ch & 7), k0[0], k0[1], k0[2],
+                    k0[3]);
+            ldsm_x4(stK + (ch >> 3) * kHalfBytes + swz128(8 + (lane & 7), ch & 7), k1[0], k1[1],
+                    k1[2], k1[3]);
+            // k-step 2 sp (dims 32 sp .. +15) and 2 sp + 1 (dims 32 sp + 16 .. +31)
+            mma_16816(sa, k0[0], k1[0], k0[1], k1[1], qb0[2 * sp], qb1[2 * sp]);
+            mma_16816(sb2, k0[2], k1[2], k0[3], k1[3], qb0[2 * sp + 1], qb1[2 * sp + 1]);
+          }
+          // ---- mask, online softmax over this thread's rows (exp2 domain) ----
+          // sa: [0] key g row 2t4, [1] key g row 2t4+1, [2] key g+8 row 2t4, [3] key g+8 row 2t4+1
+          float pv[4];
+          float alpha[2];
+          bool rescale = false;
+          // positions of keys g and g + 8 (ring: the positions their slots hold)
+          const int pos0 = RING ? ring_pos(a, c * kChunk + g, lo_pos, r_lo) : c * kChunk + g;
+          const int pos1 = RING ? ring_pos(a, c * kChunk + g + 8, lo_pos, r_lo) : c * kChunk + g + 8;
+  #pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float x0 = (sa[e] + sb2[e]) * score_l2;
+            float x1 = (sa[2 + e] + sb2[2 + e]) * score_l2;
+            if (!full_chunk) {
+              x0 = pos0 < tlim[e] ? x0 : kNegInf;
+              x1 = pos1 < tlim[e] ? x1 : kNegInf;
+            }
+            float mx = fmaxf(x0, x1);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_old = tm[e];
+            const float m_new = fmaxf(m_old, mx);
+            const float m_use = m_new == kNegInf ? 0.f : m_new;
+            alpha[e] = fast_exp2(m_old - m_use);
+            rescale |= (m_old != kNegInf) && (m_new != m_old);
+            tm[e] = m_new;
+            pv[e] = fast_exp2(x0 - m_use);
+            pv[2 + e] = fast_exp2(x1 - m_use);
+            tl[e] = tl[e] * alpha[e] + (pv[e] + pv[2 + e]);
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+  #pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+              ot[dt][0] *= alpha[0];
+              ot[dt][1] *= alpha[1];
+              ot[dt][2] *= alpha[0];
+              ot[dt][3] *= alpha[1];
+            }
+          }
+          // P^T (keys x rows) to the B operand (rows g, keys 2t4..): transpose the two 8x8 halves
+          const uint32_t pb0 = movmatrix_trans(pack_half2(pv[0], pv[1]));
+          const uint32_t pb1 = movmatrix_trans(pack_half2(pv[2], pv[3]));
+          // tokens no query may see may hold anything, NaN included: zero their V entries
+          uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+          if (!full_chunk) {
+            const int t0 = c * kChunk + 2 * t4;
+            if (RING) {
+              vm0 = (ring_pos(a, t0, lo_pos, r_lo) < Lc ? 0x0000ffffu : 0u) |
+                    (ring_pos(a, t0 + 1, lo_pos, r_lo) < Lc ? 0xffff0000u : 0u);
+              vm1 = (ring_pos(a, t0 + 8, lo_pos, r_lo) < Lc ? 0x0000ffffu : 0u) |
+                    (ring_pos(a, t0 + 9, lo_pos, r_lo) < Lc ? 0xffff0000u : 0u);
+            } else {
+              vm0 = (t0 < Lc ? 0x0000ffffu : 0u) | (t0 + 1 < Lc ? 0xffff0000u : 0u);
+              vm1 = (t0 + 8 < Lc ? 0x0000ffffu : 0u) | (t0 + 9 < Lc ? 0xffff0000u : 0u);
+            }
+          }
+          // ---- O^T += V^T P^T: V fragments as the A operand ----
+  #pragma unroll
+          for (int dt = 0; dt < 8; ++dt) {
+            const int i = lane >> 3;
+            const int tok = (i & 1) * 8 + (lane & 7);
+            const int ch = 2 * dt + (i >> 1);
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_trans(stV + (ch >> 3) * kHalfBytes + swz128(tok, ch & 7), v0, v1, v2, v3);
+            v0 &= vm0; v1 &= vm1; v2 &= vm0; v3 &= vm1;
+            mma_16816(ot[dt], v0, v2, v1, v3, pb0, pb1);
+          }
+          if (RING || (APPEND && patched)) fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_empty + st * 8);
         }
@@ -1182,7 +1286,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_qempty + qs * 8);
       }
-      j += nchunk;
+      j += FP8 ? (nchunk + 1) >> 1 : nchunk;   // stages of the segment
       // ---- hand this warp's state to the epilogue: rows 2t4, 2t4 + 1 ----
       const int sb = k & 1;
       if (k >= 2 && !mbar_wait(bar_sfree + sb * 8, ((k >> 1) - 1) & 1, abort)) flag_timeout(a, abort);
@@ -1195,11 +1299,22 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         lv += __shfl_xor_sync(0xffffffffu, lv, 16);
         const int r = 2 * t4 + e;
         if (r < a.R) {
-          float* dst = o_d + (w * a.R + r) * kSt + g;
+          float* row = o_d + (w * a.R + r) * kSt;
+          if constexpr (FP8) {
+            // dims 16 g + dt (tile rows g) and 16 g + 8 + dt (rows g + 8), scaled by the V scale
+            float4* dst = reinterpret_cast<float4*>(row + 16 * g);
+            dst[0] = make_float4(ot[0][e] * out_sc, ot[1][e] * out_sc, ot[2][e] * out_sc, ot[3][e] * out_sc);
+            dst[1] = make_float4(ot[4][e] * out_sc, ot[5][e] * out_sc, ot[6][e] * out_sc, ot[7][e] * out_sc);
+            dst[2] = make_float4(ot[0][2 + e] * out_sc, ot[1][2 + e] * out_sc, ot[2][2 + e] * out_sc,
+                                 ot[3][2 + e] * out_sc);
+            dst[3] = make_float4(ot[4][2 + e] * out_sc, ot[5][2 + e] * out_sc, ot[6][2 + e] * out_sc,
+                                 ot[7][2 + e] * out_sc);
+          } else {
 #pragma unroll
-          for (int dt = 0; dt < 8; ++dt) {
-            dst[16 * dt] = FP8 ? ot[dt][e] * out_sc : ot[dt][e];
-            dst[16 * dt + 8] = FP8 ? ot[dt][2 + e] * out_sc : ot[dt][2 + e];
+            for (int dt = 0; dt < 8; ++dt) {
+              row[g + 16 * dt] = ot[dt][e];
+              row[g + 16 * dt + 8] = ot[dt][2 + e];
+            }
           }
           if (g == 0) {
             stM[(sb * NCW + w) * a.R + r] = tm[e];
@@ -1568,14 +1683,15 @@ constexpr int kNCWRing = 4, kNSTRing = 8;
 #define PKV_RING_TR_STAGES 12
 #endif
 constexpr int kNCWRingTR = PKV_RING_TR_WARPS, kNSTRingTR = PKV_RING_TR_STAGES;
-// The E4M3 cache: 4 KB stages plus a 4 KB fp16 V tile per consumer warp, within the shared
-// memory of the fp16 kernels (two CTAs per SM). Widening the codes adds to each consumer warp's
-// work, so four consumer warps share the chunks (twelve stages, 48 KB of K/V in flight per CTA).
+// The E4M3 cache: 8 KB stages of two chunks each (the producer's per-stage work, and the
+// consumers' per-softmax-step work, spread over twice the keys of an fp16 stage's bytes), two
+// CTAs per SM. Widening the codes adds to each consumer warp's work, so four consumer warps
+// share the stages (eight stages, 64 KB of K/V in flight per CTA).
 #ifndef PKV_FP8_WARPS
 #define PKV_FP8_WARPS 4
 #endif
 #ifndef PKV_FP8_STAGES
-#define PKV_FP8_STAGES 12
+#define PKV_FP8_STAGES 8
 #endif
 constexpr int kNCWFp8 = PKV_FP8_WARPS, kNSTFp8 = PKV_FP8_STAGES;
 
