@@ -481,12 +481,11 @@ __device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// E4M3 pair (low byte first) -> fp16 pair, exact (every E4M3 value is an fp16 value).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
-  uint32_t y;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-      : "=r"(y) : "r"(x));
-  return y;
+// Four E4M3 codes -> two fp16 pairs: bytes 0-1 into lo, bytes 2-3 into hi (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(x));
 }
 
 // Ring: rotate-half RoPE of one chunk's 16 keys by their cache index, in place in the chunk's K
@@ -1030,8 +1029,29 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             __syncwarp();
             patched = true;
           }
-          // ---- S^T = K Q^T for both chunks: keys g and g + 8 of each, one word of four codes
-          // per 16-dim step, widened in registers; two chains per chunk ----
+          // ---- the stage's codes into registers, then the stage goes back to the producer:
+          // K, keys g and g + 8 of each chunk, one word of four codes per 16-dim step; V, dims
+          // 16 g .. 16 g + 15 of keys 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9 of each chunk (the
+          // output dims of rows g and g + 8 of the PV tiles below) ----
+          uint32_t kw[2][8][2];
+          uint4 vr[2][4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              kw[h][ks][0] = ld_shared_u32(stK + swz128(16 * h + g, ks) + 4 * t4);
+              kw[h][ks][1] = ld_shared_u32(stK + swz128(16 * h + g + 8, ks) + 4 * t4);
+            }
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              vr[h][i] = ld_shared_v4(stVc + swz128(16 * h + 2 * t4 + (i & 1) + 8 * (i >> 1), g));
+          if (APPEND && patched) fence_proxy_async_smem();
+          __syncwarp();                      // every code of the stage has been read
+          if (lane == 0) mbar_arrive(bar_empty + st * 8);
+          // ---- S^T = K Q^T for both chunks, the codes widened in registers; two chains per
+          // chunk ----
           float sa[2][4], sb[2][4];
 #pragma unroll
           for (int h = 0; h < 2; ++h)
@@ -1041,27 +1061,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const uint32_t w0 = ld_shared_u32(stK + swz128(16 * h + g, ks) + 4 * t4);
-              const uint32_t w1 = ld_shared_u32(stK + swz128(16 * h + g + 8, ks) + 4 * t4);
-              const uint32_t a0 = e4m3x2_to_f16x2(w0), a2 = e4m3x2_to_f16x2(w0 >> 16);
-              const uint32_t a1 = e4m3x2_to_f16x2(w1), a3 = e4m3x2_to_f16x2(w1 >> 16);
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x4(kw[h][ks][0], a0, a2);
+              e4m3x4_to_f16x4(kw[h][ks][1], a1, a3);
               if (ks & 1)
                 mma_16816(sb[h], a0, a1, a2, a3, qb0[ks], qb1[ks]);
               else
                 mma_16816(sa[h], a0, a1, a2, a3, qb0[ks], qb1[ks]);
             }
           }
-          // V codes: dims 16 g .. 16 g + 15 of keys 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9 of each
-          // chunk (the output dims of rows g and g + 8 of the PV tiles below)
-          uint4 vr[2][4];
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              vr[h][i] = ld_shared_v4(stVc + swz128(16 * h + 2 * t4 + (i & 1) + 8 * (i >> 1), g));
-          if (APPEND && patched) fence_proxy_async_smem();
-          __syncwarp();                      // every code of the stage has been read
-          if (lane == 0) mbar_arrive(bar_empty + st * 8);
 
           // ---- mask, online softmax over this thread's rows and 4 keys (exp2 domain) ----
           float pv[2][4], alpha[2];
@@ -1141,15 +1149,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
               const uint32_t lo89 = __byte_perm(u4_word(vr[h][2], wi), u4_word(vr[h][3], wi), sel);
               const uint32_t hi89 =
                   __byte_perm(u4_word(vr[h][2], wi + 2), u4_word(vr[h][3], wi + 2), sel);
+              uint32_t a0[2], a1[2], a2[2], a3[2];   // [e]: dims 2 dp + e
+              e4m3x4_to_f16x4(lo01, a0[0], a0[1]);
+              e4m3x4_to_f16x4(hi01, a1[0], a1[1]);
+              e4m3x4_to_f16x4(lo89, a2[0], a2[1]);
+              e4m3x4_to_f16x4(hi89, a3[0], a3[1]);
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int sh = 16 * e;
-                const uint32_t a0 = e4m3x2_to_f16x2(lo01 >> sh) & vm[h][0];
-                const uint32_t a1 = e4m3x2_to_f16x2(hi01 >> sh) & vm[h][0];
-                const uint32_t a2 = e4m3x2_to_f16x2(lo89 >> sh) & vm[h][1];
-                const uint32_t a3 = e4m3x2_to_f16x2(hi89 >> sh) & vm[h][1];
-                mma_16816(ot[2 * dp + e], a0, a1, a2, a3, pb[h][0], pb[h][1]);
-              }
+              for (int e = 0; e < 2; ++e)
+                mma_16816(ot[2 * dp + e], a0[e] & vm[h][0], a1[e] & vm[h][0], a2[e] & vm[h][1],
+                          a3[e] & vm[h][1], pb[h][0], pb[h][1]);
             }
           }
         }
