@@ -253,70 +253,73 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   } else if (warp == 1) {
     // =================================== MMA issue =============================================
     // Order: S_0(0), S_1(0); then per key tile j and query tile i: P_i(j) V_j, S_i(j + 1). A
-    // commit tracks every MMA this thread issued before it, so when S_i(j + 1) is done
+    // commit tracks every MMA its thread issued before it, so when S_i(j + 1) is done
     // (s_full_i) P_i(j) V_j is too: the softmax of tile i may then overwrite P_i (written over
     // S_i) and rescale O_i. While one tile's softmax runs, the tensor core works on the other.
     // Q and P come from tensor memory: only K and V are read from shared memory.
-    if (lane == 0) {
-      constexpr uint32_t idS = tc_idesc_f16(kM, kKT, false);
-      constexpr uint32_t idO = tc_idesc_f16(kM, kD, true);
-      const int nk[2] = {nkt0, has1 ? nkt1 : 0};
-      bool ok = nkt == 0 || mbar_wait_ns(bar_q_tmem, 0, abort, kWaitNs);
-      if (!ok) flag_timeout(a, abort);
-      int waited = -1;                       // key tiles whose stage is known to have landed
-      auto wait_kv = [&](int j) -> bool {
-        while (waited < j) {
-          const int jj = waited + 1;
-          if (!mbar_wait_ns(bar_kv_full + (jj % kNS) * 8, (jj / kNS) & 1, abort, kWaitNs))
-            return false;
-          waited = jj;
-        }
-        return true;
-      };
-      auto issue_s = [&](int i, int j) {
-        const uint32_t kst = sb0 + kStage0 + (j % kNS) * kStageBytes;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t koff = (ks >> 2) * 8192 + (ks & 3) * 32;   // K lo/hi half
-          // Q from tensor memory: 16 dims = 8 columns per step
-          tc_mma_f16_ts(tmem + i * kKT, tmem + kTmQ + i * kKT + ks * 8,
-                        tc_desc_sw128(kst + koff, 16, 1024), idS, ks > 0);
-        }
-        tc_commit(bar_s_full + i * 8);
-      };
-      for (int i = 0; ok && i < 2; ++i) {
-        if (nk[i] == 0) continue;
-        if (!(ok = wait_kv(0))) break;
-        issue_s(i, 0);
+    // The whole warp runs this loop (uniform control flow, every wait decided for the warp) and
+    // one elected lane, the same every time, issues each MMA and commit: issued from a single
+    // thread's branch, back-to-back MMAs with addresses computed in the loop went out at about
+    // a third of the tensor core's rate.
+    constexpr uint32_t idS = tc_idesc_f16(kM, kKT, false);
+    constexpr uint32_t idO = tc_idesc_f16(kM, kD, true);
+    const int nk[2] = {nkt0, has1 ? nkt1 : 0};
+    auto wwait = [&](uint32_t bar, uint32_t parity, const volatile int* ab) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait_ns(bar, parity, ab, kWaitNs));
+    };
+    bool ok = nkt == 0 || wwait(bar_q_tmem, 0, abort);
+    int waited = -1;                         // key tiles whose stage is known to have landed
+    auto wait_kv = [&](int j) -> bool {
+      while (waited < j) {
+        const int jj = waited + 1;
+        if (!wwait(bar_kv_full + (jj % kNS) * 8, (jj / kNS) & 1, abort)) return false;
+        waited = jj;
       }
-      for (int j = 0; ok && j < nkt; ++j) {
-        for (int i = 0; i < 2; ++i) {
-          if (j >= nk[i]) continue;
-          if (!(ok = mbar_wait_ns(bar_p_full + i * 8, j & 1, abort, kWaitNs))) break;
-          tc_fence_after();
-          const uint32_t vst = sb0 + kStage0 + (j % kNS) * kStageBytes + 16384;
+      return true;
+    };
+    auto issue_s = [&](int i, int j) {
+      const uint32_t kst = sb0 + kStage0 + (j % kNS) * kStageBytes;
+      tc_fence_after();
 #pragma unroll
-          for (int kt = 0; kt < 4; ++kt) {
-            // P from tensor memory (16 keys = 8 columns per step, over S_i); V: MN-major, 16
-            // keys = two 8-row groups (1024 B apart), the dims' 64-column halves 8 KB apart
-            tc_mma_f16_ts(tmem + kTmO + i * kD, tmem + i * kKT + kt * 8,
-                          tc_desc_sw128(vst + kt * 2048, 8192, 1024), idO, (j > 0 || kt > 0));
-          }
-          if (j + 1 < nk[i]) {
-            if (!(ok = wait_kv(j + 1))) break;
-            issue_s(i, j + 1);
-          }
-        }
-        if (!ok) break;
-        tc_commit(bar_kv_empty + (j % kNS) * 8);   // both tiles' P V of key tile j issued
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (ks >> 2) * 8192 + (ks & 3) * 32;   // K lo/hi half
+        // Q from tensor memory: 16 dims = 8 columns per step
+        tc_mma_f16_ts_elect(tmem + i * kKT, tmem + kTmQ + i * kKT + ks * 8,
+                            tc_desc_sw128(kst + koff, 16, 1024), idS, ks > 0);
       }
-      if (!ok) flag_timeout(a, abort);
-      // every MMA issued (all of them on the normal path) has completed when o_final fires
-      tc_commit(bar_o_final);
-      if (!mbar_wait_ns(bar_o_final, 0, nullptr, kWaitNs)) flag_timeout(a, abort);
+      tc_commit_elect(bar_s_full + i * 8);
+    };
+    for (int i = 0; ok && i < 2; ++i) {
+      if (nk[i] == 0) continue;
+      if (!(ok = wait_kv(0))) break;
+      issue_s(i, 0);
     }
-    __syncwarp();
+    for (int j = 0; ok && j < nkt; ++j) {
+      for (int i = 0; i < 2; ++i) {
+        if (j >= nk[i]) continue;
+        if (!(ok = wwait(bar_p_full + i * 8, j & 1, abort))) break;
+        tc_fence_after();
+        const uint32_t vst = sb0 + kStage0 + (j % kNS) * kStageBytes + 16384;
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+          // P from tensor memory (16 keys = 8 columns per step, over S_i); V: MN-major, 16
+          // keys = two 8-row groups (1024 B apart), the dims' 64-column halves 8 KB apart
+          tc_mma_f16_ts_elect(tmem + kTmO + i * kD, tmem + i * kKT + kt * 8,
+                              tc_desc_sw128(vst + kt * 2048, 8192, 1024), idO,
+                              (j > 0 || kt > 0));
+        }
+        if (j + 1 < nk[i]) {
+          if (!(ok = wait_kv(j + 1))) break;
+          issue_s(i, j + 1);
+        }
+      }
+      if (!ok) break;
+      tc_commit_elect(bar_kv_empty + (j % kNS) * 8);   // both tiles' P V of key tile j issued
+    }
+    if (!ok && lane == 0) flag_timeout(a, abort);
+    // every MMA issued (all of them on the normal path) has completed when o_final fires
+    tc_commit_elect(bar_o_final);
+    if (!wwait(bar_o_final, 0, nullptr) && lane == 0) flag_timeout(a, abort);
   } else {
     // =================================== softmax ===============================================
     // Warps 2-5 take query tile 0, warps 6-9 tile 1, one thread per row. tcgen05.ld / st are
