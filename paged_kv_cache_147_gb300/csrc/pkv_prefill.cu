@@ -314,7 +314,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
       }
       if (!ok) break;
-      tc_commit_elect(bar_kv_empty + (j % kNS) * 8);   // both tiles' P V of key tile j issued
+      // both tiles' P V of key tile j issued (a commit between them costs more than the stage
+      // comes back earlier)
+      tc_commit_elect(bar_kv_empty + (j % kNS) * 8);
     }
     if (!ok && lane == 0) flag_timeout(a, abort);
     // every MMA issued (all of them on the normal path) has completed when o_final fires
@@ -381,17 +383,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // times the (positive) scale is the maximum of the scaled ones
 #pragma unroll
         for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(sr[i]);
-        float r0 = x[0];
+        // a tree (8 chains of 8, then 3 levels): this reduction is on the tile's critical path
+        float r8[8];
 #pragma unroll
-        for (int i = 1; i < 64; ++i) r0 = sl_pos ? fmaxf(r0, x[i]) : fminf(r0, x[i]);
-        mx = r0 * a.scale_log2;
+        for (int k = 0; k < 8; ++k) r8[k] = x[k];
+#pragma unroll
+        for (int i = 8; i < 64; i += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            r8[k] = sl_pos ? fmaxf(r8[k], x[i + k]) : fminf(r8[k], x[i + k]);
+#pragma unroll
+        for (int w2 = 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+          for (int k = 0; k < w2; ++k)
+            r8[k] = sl_pos ? fmaxf(r8[k], r8[k + w2]) : fminf(r8[k], r8[k + w2]);
+        mx = r8[0] * a.scale_log2;
       } else {
 #pragma unroll
         for (int i = 0; i < 64; ++i)
           x[i] = base + i < lim ? __uint_as_float(sr[i]) * a.scale_log2 : kNegInf;
-        mx = x[0];
+        float r8[8];
 #pragma unroll
-        for (int i = 1; i < 64; ++i) mx = fmaxf(mx, x[i]);
+        for (int k = 0; k < 8; ++k) r8[k] = x[k];
+#pragma unroll
+        for (int i = 8; i < 64; i += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) r8[k] = fmaxf(r8[k], x[i + k]);
+#pragma unroll
+        for (int w2 = 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+          for (int k = 0; k < w2; ++k) r8[k] = fmaxf(r8[k], r8[k + w2]);
+        mx = r8[0];
       }
       const bool raise = mx > m_used + kLazy;
       const bool resc = raise && m_used != kNegInf;   // this row's O and l need rescaling
@@ -411,24 +433,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       if (raise) m_used = mx;
       const float m_use = m_used == kNegInf ? 0.f : m_used;
       uint32_t ph[32];
-      float rs = 0.f;
+      float rs[2] = {0.f, 0.f};                 // two partial sums: a shorter dependent chain
       if (unmasked) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float p0 = fast_exp2(fmaf(x[2 * i], a.scale_log2, -m_use));
           const float p1 = fast_exp2(fmaf(x[2 * i + 1], a.scale_log2, -m_use));
-          rs += p0 + p1;
+          rs[i & 1] += p0 + p1;
           ph[i] = pack_half2(p0, p1);
         }
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float p0 = fast_exp2(x[2 * i] - m_use), p1 = fast_exp2(x[2 * i + 1] - m_use);
-          rs += p0 + p1;
+          rs[i & 1] += p0 + p1;
           ph[i] = pack_half2(p0, p1);
         }
       }
-      l += rs;
+      l += rs[0] + rs[1];
       // the last box loaded ends at kpad; its rows at or past the context end may hold
       // anything: zero them in V before P V reads them (P is 0 there, but 0 x NaN is not).
       // Both groups zero the same rows when both use the tile (the same bytes).
