@@ -155,6 +155,7 @@ def _new_slots(tables, lens, q_len, bs):
     ([33, 16, 2, 100], 16, 8, 4, 2),                     # causal pairs, new rows across blocks
     ([64, 5, 31, 4], 16, 4, 4, 4),                       # MHA drafts (R = 4)
     ([500, 70, 1], 64, 16, 2, 1),                        # 64-token blocks
+    ([18, 50, 97, 16], 16, 8, 4, 4),                     # drafts across both chunks of a stage
 ])
 def test_fused_append_decode_fp8_matches_oracle(lens, bs, hq, hkv, q_len):
     k8, v8, ks, vs, tables, lens, q = _fp8_case(lens, bs, hq, hkv, q_len, seed=len(lens) * 7 + q_len)
