@@ -16,14 +16,15 @@
 //  * Keys in 64-token tiles: S = Q K^T (M 128, N 64, K 128) into tensor memory, then after the
 //    softmax O += P V (M 128, N 128, K 64), with Q and P read from tensor memory (only K and V
 //    come from shared memory, whose bandwidth the MMAs would otherwise saturate) and O
-//    accumulated there for the whole context: tcgen05.mma kind::f16, f32 accumulate, issued
-//    by one thread.
+//    accumulated there for the whole context: tcgen05.mma kind::f16, f32 accumulate.
 //  * Warp roles: warp 0 loads (TMA: the query tiles once, then K and V of each key tile as
 //    16-token boxes at the rows the block table gives, into a 4-deep ring of 32 KB stages);
 //    warp 1 allocates tensor memory (512 columns: S, O and Q of each tile) and issues the
-//    MMAs; warps 2-5 and 6-9 copy their query rows into tensor memory, then run the online
-//    softmax of tile 0 and tile 1, one thread per row: S from tensor memory, mask, exp2 (the
-//    score scale folded into its argument), P (fp16) written back over S for the next MMA.
+//    MMAs, the whole warp running the issue loop and one elected lane issuing; warps 2-5 and
+//    6-9 copy their query rows into tensor memory, then run the online softmax of tile 0 and
+//    tile 1, one thread per row: S from tensor memory, mask, the row maximum by a tree, exp2
+//    (the score scale folded into its argument), P (fp16) written back over S for the next
+//    MMA.
 //    The MMA order alternates the tiles (P_i(j) V_j, then S_i(j + 1)), so the tensor core works
 //    on one tile while the other tile's softmax runs.
 //  * The running maximum is raised only when a row's maximum grows by more than 2^8: the
