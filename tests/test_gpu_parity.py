@@ -104,6 +104,7 @@ def test_llama70b_sampled_layers(make):
 
 @pytest.mark.parametrize("make,layers", [(workloads.tiny, (0,)),
                                          (workloads.edge_1p1b, tuple(range(24))),
+                                         (workloads.llama70b_b16, (0, 1, 40, 79)),
                                          (workloads.llama70b_mixed, (0, 79))])
 def test_fused_append_decode(make, layers):
     w = make()
@@ -292,6 +293,32 @@ def test_ring_multi_layer_pool_at_layer_stride(fused):
     for layer in range(3):
         assert np.array_equal(u16(k_all[layer]), hosts[layer][0].view(np.uint16)), layer
         assert np.array_equal(u16(v_all[layer]), hosts[layer][1].view(np.uint16)), layer
+
+
+def test_ring_every_layer_of_the_benchmark_pool():
+    """The benchmark's ring step through the fused calls on all 24 layers of its pool: per
+    layer the 4 drafts appended and decoded, a rollback of 2, one more token appended and
+    decoded; every layer's bytes and every output against the oracle."""
+    w = workloads.ring(num_layers=24)
+    k_all, v_all = w.pools(DEV)
+    bt_d = _dev(w.block_tables, torch.int32)
+    rope_d = pkv.rope_table(w.sink + w.window).to(DEV)
+    ws = pkv.make_workspace(w.num_seqs, 4, w.num_q_heads, w.num_kv_heads)
+    L0 = w.ring_len0.astype(np.int64)
+    hw = L0 + 4
+    for layer in range(w.num_layers):
+        k_host, v_host = f16_host(k_all[layer]).copy(), f16_host(v_all[layer]).copy()
+        kn, vn = w.new_kv(layer, DEV)
+        q = w.query(layer, DEV)
+        out, ref = _ring_step(w, k_all[layer], v_all[layer], bt_d, rope_d, ws, k_host, v_host,
+                              L0 + 4, hw, 4, kn, vn, q, fused=True)
+        assert_attn_close(out, ref, f"ring drafts, layer {layer}")
+        kn1 = w.draw((w.num_seqs, 2, 128), layer, 100, DEV)
+        vn1 = w.draw((w.num_seqs, 2, 128), layer, 101, DEV)
+        q1 = w.draw((w.num_seqs, 1, 12, 128), layer, 102, DEV)
+        out, ref = _ring_step(w, k_all[layer], v_all[layer], bt_d, rope_d, ws, k_host, v_host,
+                              L0 + 3, hw, 1, kn1, vn1, q1, fused=True)
+        assert_attn_close(out, ref, f"ring after rollback, layer {layer}")
 
 
 # ------------------------------------------------------------------------------ invariants
