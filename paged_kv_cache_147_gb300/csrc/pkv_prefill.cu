@@ -385,19 +385,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(sr[i]);
         // a tree (8 chains of 8, then 3 levels): this reduction is on the tile's critical path
+        // (the scale's sign, one decision for the launch, picks max or min outside the tree)
         float r8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) r8[k] = x[k];
+        if (sl_pos) {
 #pragma unroll
-        for (int i = 8; i < 64; i += 8)
+          for (int i = 8; i < 64; i += 8)
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            r8[k] = sl_pos ? fmaxf(r8[k], x[i + k]) : fminf(r8[k], x[i + k]);
+            for (int k = 0; k < 8; ++k) r8[k] = fmaxf(r8[k], x[i + k]);
 #pragma unroll
-        for (int w2 = 4; w2 >= 1; w2 >>= 1)
+          for (int w2 = 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
-          for (int k = 0; k < w2; ++k)
-            r8[k] = sl_pos ? fmaxf(r8[k], r8[k + w2]) : fminf(r8[k], r8[k + w2]);
+            for (int k = 0; k < w2; ++k) r8[k] = fmaxf(r8[k], r8[k + w2]);
+        } else {
+#pragma unroll
+          for (int i = 8; i < 64; i += 8)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) r8[k] = fminf(r8[k], x[i + k]);
+#pragma unroll
+          for (int w2 = 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+            for (int k = 0; k < w2; ++k) r8[k] = fminf(r8[k], r8[k + w2]);
+        }
         mx = r8[0] * a.scale_log2;
       } else {
 #pragma unroll
