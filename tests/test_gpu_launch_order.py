@@ -6,6 +6,8 @@ context lengths with its own device op, or that copies a shared block (copy-on-w
 before the fused call, must switch that overlap off (pkv_set_early_start(0)); these tests run
 exactly those orderings with the overlap off and hold the results to the oracle.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -87,3 +89,47 @@ def test_copy_on_write_right_before_the_fused_call(no_early_start):
     ref = oracle.paged_attention(f16_host(q), k_host, v_host, tables, w.context_lens,
                                  w.block_size, w.scale)
     assert_attn_close(out, ref, "copy-on-write then fused append + decode")
+
+
+def test_fp8_fused_call_after_lengths_advanced_on_device(no_early_start):
+    """The E4M3 fused append + decode right after a torch kernel advances the lengths."""
+    rng = np.random.default_rng(21)
+    lens = np.array([37, 100, 16, 1, 250], np.int32)         # after this step's append
+    bs, hq, hkv = 16, 12, 2
+    nblk = [(int(L) + bs - 1) // bs for L in lens]
+    nb = sum(nblk) + 2
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = np.full((len(lens), max(nblk)), -1, np.int32)
+    cur = 0
+    for b, n in enumerate(nblk):
+        tables[b, :n] = perm[cur:cur + n]
+        cur += n
+    kf = rng.standard_normal((nb, hkv, bs, 128)).astype(np.float32)
+    vf = rng.standard_normal((nb, hkv, bs, 128)).astype(np.float32)
+    ks = (np.abs(kf).max(axis=(0, 2, 3)) / 448.0).astype(np.float32)
+    vs = (np.abs(vf).max(axis=(0, 2, 3)) / 448.0).astype(np.float32)
+    k8 = torch.from_numpy(kf / ks[None, :, None, None]).clamp(-448, 448).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    v8 = torch.from_numpy(vf / vs[None, :, None, None]).clamp(-448, 448).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    q = rng.standard_normal((len(lens), 1, hq, 128)).astype(np.float16)
+    kn = rng.standard_normal((len(lens), hkv, 128)).astype(np.float16)
+    vn = rng.standard_normal((len(lens), hkv, 128)).astype(np.float16)
+    k8_d, v8_d = torch.from_numpy(k8).to(DEV), torch.from_numpy(v8).to(DEV)
+    qd, knd, vnd = (torch.from_numpy(x).to(DEV) for x in (q, kn, vn))
+    ks_d, vs_d = torch.from_numpy(ks).to(DEV), torch.from_numpy(vs).to(DEV)
+    bt = torch.from_numpy(tables).to(DEV)
+    cl = torch.from_numpy(lens - 1).to(DEV)
+    ws = pkv.make_workspace(len(lens), 1, hq, hkv)
+    out = torch.empty_like(qd)
+    scale = 1 / math.sqrt(128)
+    torch.cuda.synchronize()
+    cl.add_(1)
+    pkv.paged_attn_decode_append_fp8(out, qd, knd, vnd, k8_d, v8_d, ks_d, vs_d, bt, cl, scale, ws)
+    torch.cuda.synchronize()
+    seq = np.arange(len(lens), dtype=np.int32)
+    slots = oracle.slot_mapping(seq, (lens - 1).astype(np.int64), tables, bs)
+    oracle.kv_append_fp8(kn, vn, slots, k8, v8, bs, ks, vs)
+    assert np.array_equal(k8_d.cpu().numpy(), k8) and np.array_equal(v8_d.cpu().numpy(), v8)
+    ref = oracle.paged_attention_fp8(q, k8, v8, ks, vs, tables, lens, bs, scale)
+    assert_attn_close(out, ref, "fp8 fused after lengths advanced on the device")
