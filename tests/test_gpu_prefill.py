@@ -108,3 +108,39 @@ def test_prefill_single_token_chunk_equals_decode():
     ref = oracle.paged_attention(f16_host(q), k_host, v_host, w.block_tables, w.context_lens,
                                  w.block_size, w.scale)
     assert_attn_close(out, ref, "prefill q_len=1")
+
+
+def test_prefill_bad_block_id_sets_the_error_bit_without_fault():
+    # a table entry past the pool: that block reads as zeros (an out-of-range box), the
+    # block-id bit is set, and the other sequence's outputs are unaffected
+    w = workloads.prefill(11, [300, 129], 128, 16, 2, 16)
+    k, v = w.pools(DEV, poison=True)
+    k_host, v_host, _ = _append_chunk(w, k, v)
+    tables = w.block_tables.copy()
+    tables[1, 2] = w.num_blocks + 7
+    q = w.query(0, DEV)
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_prefill(out, q, k[0], v[0], torch.as_tensor(tables, device=DEV),
+                      torch.as_tensor(w.context_lens, device=DEV), w.scale)
+    torch.cuda.synchronize()
+    assert pkv.device_error(clear=True) & pkv.DEVERR_BLOCK_ID
+    assert torch.isfinite(out[1]).all()
+    ref = oracle.paged_attention(f16_host(q), k_host, v_host, w.block_tables, w.context_lens,
+                                 w.block_size, w.scale)
+    assert_attn_close(out[:1], ref[:1], "prefill beside a sequence with a bad block id")
+
+
+def test_prefill_context_past_the_table_is_clamped_and_flagged():
+    w = workloads.prefill(12, [100, 60], 32, 12, 2, 16)
+    k, v = w.pools(DEV, poison=True)
+    k_host, v_host, bt = _append_chunk(w, k, v)
+    lens = w.context_lens.copy()
+    lens[1] = w.block_tables.shape[1] * w.block_size + 50      # past the end of its table
+    q = w.query(0, DEV)
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_prefill(out, q, k[0], v[0], bt, torch.as_tensor(lens, device=DEV), w.scale)
+    torch.cuda.synchronize()
+    assert pkv.device_error(clear=True) & pkv.DEVERR_CONTEXT
+    ref = oracle.paged_attention(f16_host(q), k_host, v_host, w.block_tables, w.context_lens,
+                                 w.block_size, w.scale)
+    assert_attn_close(out[:1], ref[:1], "prefill beside a sequence whose context is clamped")
