@@ -68,3 +68,29 @@ def test_spec_verify_matches_oracle(B, K, V, noise, masked):
             assert w[v] > 0 and lo - 1e-5 * cdf[-1] <= thr <= cdf[v] + 1e-5 * cdf[-1], (b, v)
     assert np.mean(nt_g == nt_o) > 0.95 and np.mean(n_g == n_o) > 0.95
     assert pkv.device_error(clear=True) == 0
+
+
+def test_out_of_range_draft_is_rejected_and_flagged():
+    """A draft token outside the vocabulary (a caller's bug) stops that sequence's accepted
+    run there and sets the token bit, without a fault; the other sequences are unaffected."""
+    rng = np.random.default_rng(5)
+    B, K, V = 6, 3, 4000
+    t = (rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32)
+    d = t[:, :K].copy()                       # identical models: every valid draft is accepted
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    x[2, 1] = V + 3
+    x[4, 0] = -1
+    ua = rng.random((B, K)).astype(np.float32)
+    us = rng.random(B).astype(np.float32)
+    n_g, nt_g = pkv.spec_verify(torch.from_numpy(t).to(DEV), torch.from_numpy(d).to(DEV),
+                                torch.from_numpy(x).to(DEV), torch.from_numpy(ua).to(DEV),
+                                torch.from_numpy(us).to(DEV))
+    torch.cuda.synchronize()
+    assert pkv.device_error(clear=True) & pkv.DEVERR_TOKEN
+    n_g, nt_g = n_g.cpu().numpy(), nt_g.cpu().numpy()
+    assert n_g[2] == 1 and n_g[4] == 0
+    assert 0 <= nt_g[2] < V and 0 <= nt_g[4] < V
+    good = [b for b in range(B) if b not in (2, 4)]
+    n_o, nt_o = oracle.spec_verify(t[good], d[good], x[good], ua[good], us[good])
+    assert np.array_equal(n_g[good], n_o)
+    assert np.array_equal(nt_g[good], nt_o)
