@@ -200,3 +200,20 @@ def test_fused_append_decode_fp8_on_the_edge_shape():
     ref = oracle.paged_attention_fp8(f16_host(q), k8, v8, ks, vs, w.block_tables, w.context_lens,
                                      w.block_size, w.scale)
     assert_attn_close(out, ref, "fp8 fused edge_1p1b")
+
+
+def test_decode_fp8_bad_block_id_sets_the_error_bit_without_fault():
+    # a table entry past the pool in the second chunk of a two-chunk stage: it reads as zeros,
+    # the block-id bit is set, and the other sequences are exact
+    k8, v8, ks, vs, tables, lens, q = _fp8_case([300, 47, 90], seed=31)
+    bad = tables.copy()
+    bad[0, 3] = k8.shape[0] + 9
+    qd = _dev(q)
+    out = torch.empty_like(qd)
+    ws = pkv.make_workspace(q.shape[0], q.shape[1], q.shape[2], k8.shape[1])
+    pkv.paged_attn_decode_fp8(out, qd, _dev(k8), _dev(v8), _dev(ks), _dev(vs),
+                              _dev(bad, torch.int32), _dev(lens, torch.int32), 0.1, ws)
+    torch.cuda.synchronize()
+    assert pkv.device_error(clear=True) & pkv.DEVERR_BLOCK_ID
+    ref = oracle.paged_attention_fp8(q, k8, v8, ks, vs, tables, lens, 16, 0.1)
+    assert_attn_close(out[1:], ref[1:], "fp8 beside a sequence with a bad block id")
