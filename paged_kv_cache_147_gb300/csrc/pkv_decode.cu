@@ -30,7 +30,9 @@
 //    or the partial. Scores and output come from mma.sync m16n8k16 (f16 in, f32 accumulate)
 //    on ldmatrix fragments of the swizzled tiles: for up to 8 rows as S^T = K Q^T and
 //    O^T = V^T P^T (keys and output dims on the mma's 16-row side), else as S = Q K^T and
-//    O = P V with the rows padded to 16 or 32. Softmax runs in the exp2 domain.
+//    O = P V with the rows padded to 16 or 32. Softmax runs in the exp2 domain; a row's
+//    running maximum is refreshed (warp shuffles, rescale) only when a score exceeds it by
+//    more than 2^8, so most steps take no warp-wide reduction.
 //  * The fused-append launch may start while its predecessor finishes (programmatic
 //    dependent launch): it requests its first stages, then waits for the predecessor before
 //    touching queries, new K/V rows, outputs and the workspace.
@@ -475,6 +477,13 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int h, in
   if (t == 0) a.counters[b * a.Hkv + h] = 0;
   merge_sync<NT>();                        // stage memory free for the next merge
 }
+
+// Online softmax: a row's running maximum m is brought up to date (a warp-wide reduction and,
+// if it grew, a rescale of l and O) only in a step where one of the row's scores exceeds m by
+// more than this many powers of two. Any m with every score <= m + kLazyLog2 gives the same
+// softmax: the weights exp2(x - m) stay <= 256, exact to fp16's relative precision, and the
+// final 1 / l and the split merges use the same m as l and O.
+constexpr float kLazyLog2 = 8.f;
 
 // Word i (0-3) of a 16-byte vector (i a compile-time constant after unrolling).
 __device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
@@ -1079,48 +1088,63 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             }
           }
 
-          // ---- mask, online softmax over this thread's rows and 4 keys (exp2 domain) ----
-          float pv[2][4], alpha[2];
-          bool rescale = false;
+          // ---- mask, online softmax over this thread's rows and 4 keys (exp2 domain). The
+          // running maximum is only brought up to date when a score exceeds it by more than
+          // kLazyLog2 (so every weight stays <= 2^kLazyLog2, exact in fp16 and fp32 alike); else
+          // the step needs no warp-wide reduction and no rescale ----
+          float pv[2][4], alpha[2] = {1.f, 1.f};
+          float x[2][2][2];   // [row e][chunk h][key g, g + 8]
+          bool grow = false;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float x[2][2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              x[h][0] = (sa[h][e] + sb[h][e]) * score_l2;           // key g of chunk c + h
-              x[h][1] = (sa[h][2 + e] + sb[h][2 + e]) * score_l2;   // key g + 8
+              x[e][h][0] = (sa[h][e] + sb[h][e]) * score_l2;           // key g of chunk c + h
+              x[e][h][1] = (sa[h][2 + e] + sb[h][2 + e]) * score_l2;   // key g + 8
               if (!full) {
                 const int p0 = (c + h) * kChunk + g;
                 const bool ok = h == 0 || two;
-                x[h][0] = ok && p0 < tlim[e] ? x[h][0] : kNegInf;
-                x[h][1] = ok && p0 + 8 < tlim[e] ? x[h][1] : kNegInf;
+                x[e][h][0] = ok && p0 < tlim[e] ? x[e][h][0] : kNegInf;
+                x[e][h][1] = ok && p0 + 8 < tlim[e] ? x[e][h][1] : kNegInf;
               }
             }
-            float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_old = tm[e];
-            const float m_new = fmaxf(m_old, mx);
-            const float m_use = m_new == kNegInf ? 0.f : m_new;
-            alpha[e] = fast_exp2(m_old - m_use);
-            rescale |= (m_old != kNegInf) && (m_new != m_old);
-            tm[e] = m_new;
+            const float lm = fmaxf(fmaxf(x[e][0][0], x[e][0][1]), fmaxf(x[e][1][0], x[e][1][1]));
+            grow |= lm > tm[e] + kLazyLog2;
+          }
+          if (__any_sync(0xffffffffu, grow)) {
+            bool rescale = false;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(fmaxf(x[e][0][0], x[e][0][1]), fmaxf(x[e][1][0], x[e][1][1]));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float m_old = tm[e];
+              const float m_new = fmaxf(m_old, mx);
+              const float m_use = m_new == kNegInf ? 0.f : m_new;
+              alpha[e] = fast_exp2(m_old - m_use);
+              rescale |= (m_old != kNegInf) && (m_new != m_old);
+              tm[e] = m_new;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+              for (int dt = 0; dt < 8; ++dt) {
+                ot[dt][0] *= alpha[0];
+                ot[dt][1] *= alpha[1];
+                ot[dt][2] *= alpha[0];
+                ot[dt][3] *= alpha[1];
+              }
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float m_use = tm[e] == kNegInf ? 0.f : tm[e];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              pv[h][e] = fast_exp2(x[h][0] - m_use);
-              pv[h][2 + e] = fast_exp2(x[h][1] - m_use);
+              pv[h][e] = fast_exp2(x[e][h][0] - m_use);
+              pv[h][2 + e] = fast_exp2(x[e][h][1] - m_use);
             }
             tl[e] = tl[e] * alpha[e] + ((pv[0][e] + pv[0][2 + e]) + (pv[1][e] + pv[1][2 + e]));
-          }
-          if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-            for (int dt = 0; dt < 8; ++dt) {
-              ot[dt][0] *= alpha[0];
-              ot[dt][1] *= alpha[1];
-              ot[dt][2] *= alpha[0];
-              ot[dt][3] *= alpha[1];
-            }
           }
           // P^T of each chunk (keys x rows) to the B operand: transpose the two 8x8 halves
           uint32_t pb[2][2];
@@ -1225,14 +1249,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             mma_16816(sa, k0[0], k1[0], k0[1], k1[1], qb0[2 * sp], qb1[2 * sp]);
             mma_16816(sb2, k0[2], k1[2], k0[3], k1[3], qb0[2 * sp + 1], qb1[2 * sp + 1]);
           }
-          // ---- mask, online softmax over this thread's rows (exp2 domain) ----
+          // ---- mask, online softmax over this thread's rows (exp2 domain); the running
+          // maximum is brought up to date only when a score exceeds it by more than kLazyLog2 ----
           // sa: [0] key g row 2t4, [1] key g row 2t4+1, [2] key g+8 row 2t4, [3] key g+8 row 2t4+1
           float pv[4];
-          float alpha[2];
-          bool rescale = false;
+          float alpha[2] = {1.f, 1.f};
           // positions of keys g and g + 8 (ring: the positions their slots hold)
           const int pos0 = RING ? ring_pos(a, c * kChunk + g, lo_pos, r_lo) : c * kChunk + g;
           const int pos1 = RING ? ring_pos(a, c * kChunk + g + 8, lo_pos, r_lo) : c * kChunk + g + 8;
+          float xs[2][2];
+          bool grow = false;
   #pragma unroll
           for (int e = 0; e < 2; ++e) {
             float x0 = (sa[e] + sb2[e]) * score_l2;
@@ -1241,28 +1267,41 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
               x0 = pos0 < tlim[e] ? x0 : kNegInf;
               x1 = pos1 < tlim[e] ? x1 : kNegInf;
             }
-            float mx = fmaxf(x0, x1);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_old = tm[e];
-            const float m_new = fmaxf(m_old, mx);
-            const float m_use = m_new == kNegInf ? 0.f : m_new;
-            alpha[e] = fast_exp2(m_old - m_use);
-            rescale |= (m_old != kNegInf) && (m_new != m_old);
-            tm[e] = m_new;
-            pv[e] = fast_exp2(x0 - m_use);
-            pv[2 + e] = fast_exp2(x1 - m_use);
-            tl[e] = tl[e] * alpha[e] + (pv[e] + pv[2 + e]);
+            xs[e][0] = x0;
+            xs[e][1] = x1;
+            grow |= fmaxf(x0, x1) > tm[e] + kLazyLog2;
           }
-          if (__any_sync(0xffffffffu, rescale)) {
+          if (__any_sync(0xffffffffu, grow)) {
+            bool rescale = false;
   #pragma unroll
-            for (int dt = 0; dt < 8; ++dt) {
-              ot[dt][0] *= alpha[0];
-              ot[dt][1] *= alpha[1];
-              ot[dt][2] *= alpha[0];
-              ot[dt][3] *= alpha[1];
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(xs[e][0], xs[e][1]);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float m_old = tm[e];
+              const float m_new = fmaxf(m_old, mx);
+              const float m_use = m_new == kNegInf ? 0.f : m_new;
+              alpha[e] = fast_exp2(m_old - m_use);
+              rescale |= (m_old != kNegInf) && (m_new != m_old);
+              tm[e] = m_new;
             }
+            if (__any_sync(0xffffffffu, rescale)) {
+  #pragma unroll
+              for (int dt = 0; dt < 8; ++dt) {
+                ot[dt][0] *= alpha[0];
+                ot[dt][1] *= alpha[1];
+                ot[dt][2] *= alpha[0];
+                ot[dt][3] *= alpha[1];
+              }
+            }
+          }
+  #pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float m_use = tm[e] == kNegInf ? 0.f : tm[e];
+            pv[e] = fast_exp2(xs[e][0] - m_use);
+            pv[2 + e] = fast_exp2(xs[e][1] - m_use);
+            tl[e] = tl[e] * alpha[e] + (pv[e] + pv[2 + e]);
           }
           // P^T (keys x rows) to the B operand (rows g, keys 2t4..): transpose the two 8x8 halves
           const uint32_t pb0 = movmatrix_trans(pack_half2(pv[0], pv[1]));
@@ -1491,57 +1530,75 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                         f[2], f[3], kf[nt][s8][0], kf[nt][s8][1]);
           }
 
-        // ---- mask, online softmax (exp2 domain) ----
+        // ---- mask, online softmax (exp2 domain); a row's running maximum is brought up to
+        // date only when one of its scores exceeds it by more than kLazyLog2 ----
         uint32_t pa[MT][4];
         float alpha[MT][2];
-        bool rescale = false;
+        float v[MT][2][4];
+        bool grow = false;
   #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
   #pragma unroll
           for (int rh = 0; rh < 2; ++rh) {
-            float v[4];
+            alpha[mt][rh] = 1.f;
   #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
   #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const float x = (kDual ? sc[mt][nt][rh * 2 + e] + sc2[kDual ? mt : 0][nt][rh * 2 + e]
                                        : sc[mt][nt][rh * 2 + e]) * a.scale_log2;
-                v[nt * 2 + e] = (full_chunk || pcol[nt][e] < lim[mt][rh]) ? x : kNegInf;
+                v[mt][rh][nt * 2 + e] = (full_chunk || pcol[nt][e] < lim[mt][rh]) ? x : kNegInf;
               }
-            float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_old = m_run[mt][rh];
-            const float m_new = fmaxf(m_old, mx);
-            const float m_use = m_new == kNegInf ? 0.f : m_new;
-            // O and l are still exactly zero while m_old is -inf, so only a finite, grown
-            // maximum needs the accumulators rescaled
-            alpha[mt][rh] = fast_exp2(m_old - m_use);
-            rescale |= (m_old != kNegInf) && (m_new != m_old);
-            m_run[mt][rh] = m_new;
-            float rs = 0.f;
-  #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              v[i] = fast_exp2(v[i] - m_use);
-              rs += v[i];
-            }
-            l_run[mt][rh] = l_run[mt][rh] * alpha[mt][rh] + rs;
-            // P as the A operand: a0/a2 hold row g, a1/a3 row g+8
-            pa[mt][rh] = pack_half2(v[0], v[1]);
-            pa[mt][2 + rh] = pack_half2(v[2], v[3]);
+            const float lm = fmaxf(fmaxf(v[mt][rh][0], v[mt][rh][1]), fmaxf(v[mt][rh][2], v[mt][rh][3]));
+            grow |= lm > m_run[mt][rh] + kLazyLog2;
           }
         }
-        if (__any_sync(0xffffffffu, rescale)) {
+        if (__any_sync(0xffffffffu, grow)) {
+          bool rescale = false;
   #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
-            for (int nd = 0; nd < 16; ++nd) {
-              o[mt][nd][0] *= alpha[mt][0];
-              o[mt][nd][1] *= alpha[mt][0];
-              o[mt][nd][2] *= alpha[mt][1];
-              o[mt][nd][3] *= alpha[mt][1];
+            for (int rh = 0; rh < 2; ++rh) {
+              float mx = fmaxf(fmaxf(v[mt][rh][0], v[mt][rh][1]), fmaxf(v[mt][rh][2], v[mt][rh][3]));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+              const float m_old = m_run[mt][rh];
+              const float m_new = fmaxf(m_old, mx);
+              const float m_use = m_new == kNegInf ? 0.f : m_new;
+              // O and l are still exactly zero while m_old is -inf, so only a finite, grown
+              // maximum needs the accumulators rescaled
+              alpha[mt][rh] = fast_exp2(m_old - m_use);
+              rescale |= (m_old != kNegInf) && (m_new != m_old);
+              m_run[mt][rh] = m_new;
             }
+          if (__any_sync(0xffffffffu, rescale)) {
+  #pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+  #pragma unroll
+              for (int nd = 0; nd < 16; ++nd) {
+                o[mt][nd][0] *= alpha[mt][0];
+                o[mt][nd][1] *= alpha[mt][0];
+                o[mt][nd][2] *= alpha[mt][1];
+                o[mt][nd][3] *= alpha[mt][1];
+              }
+          }
         }
+  #pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+  #pragma unroll
+          for (int rh = 0; rh < 2; ++rh) {
+            const float m_use = m_run[mt][rh] == kNegInf ? 0.f : m_run[mt][rh];
+            float rs = 0.f;
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              v[mt][rh][i] = fast_exp2(v[mt][rh][i] - m_use);
+              rs += v[mt][rh][i];
+            }
+            l_run[mt][rh] = l_run[mt][rh] * alpha[mt][rh] + rs;
+            // P as the A operand: a0/a2 hold row g, a1/a3 row g+8
+            pa[mt][rh] = pack_half2(v[mt][rh][0], v[mt][rh][1]);
+            pa[mt][2 + rh] = pack_half2(v[mt][rh][2], v[mt][rh][3]);
+          }
 
         // tokens no query may see (past the cache, or not in the ring's valid set) may hold
         // anything, NaN included: zero their V entries so that 0 * V stays 0
