@@ -818,7 +818,7 @@ def measure_spec_verify(args, local_rank, B=32, K=4, V=32000, seed=6):
     nt = torch.empty_like(n)
     g = capture(lambda: pkv.spec_verify(t, d, x, ua, us, n, nt))
     clocks = ClockSampler(local_rank)
-    med, reps, _, clk = time_graph(g, args.steps, args.warmup, args.min_seconds / 2, clocks)
+    med, reps, _, clk = time_graph(g, args.steps, args.warmup, args.min_seconds, clocks)
     per = med / args.steps
     nbytes = (t.numel() + d.numel()) * 4
     peak, kind = load_peaks()
