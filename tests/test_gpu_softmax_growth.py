@@ -7,7 +7,8 @@ a component along the group's query direction that rises in levels across the co
 falls back once), plus a few isolated spikes above every level, so that the maximum grows by
 far more than 2^8 in the middle of segments, of stages and of split units. The fp16 cache is
 run through the 8-row transposed tile (GQA 6 and 8, MHA with 64-token blocks), the 16-row tile
-(R = 12) and the two-m-tile form (R = 18); the E4M3 cache through its two-chunk stages.
+(R = 12) and the two-m-tile form (R = 18); the E4M3 cache through its two-chunk stages; and
+the chunked prefill, which rescales O in tensor memory past the same margin.
 Results must meet the attention bar of tests/_util.py against the fp64 oracle.
 """
 import math
@@ -143,3 +144,23 @@ def test_decode_fp8_scores_climbing_along_the_context(lens, bs, hq, hkv, q_len):
     torch.cuda.synchronize()
     ref = oracle.paged_attention_fp8(q, k8, v8, ks, vs, tables, lens, bs, SCALE)
     assert_attn_close(out, ref, f"fp8 lens={list(lens[:3])} G={hq // hkv} q_len={q_len}")
+
+
+@pytest.mark.parametrize("lens,bs,hq,hkv,q_len", [
+    ([1500, 513], 16, 12, 2, 128),            # GQA 6, 128-token chunks
+    ([4096, 700], 16, 16, 2, 512),            # GQA 8, 512-token chunks at the end of 4096
+    ([900, 300], 64, 8, 8, 64),               # MHA, 64-token blocks
+])
+def test_prefill_scores_climbing_along_the_context(lens, bs, hq, hkv, q_len):
+    """The chunked prefill raises a row's maximum, and rescales O and the row sum in tensor
+    memory, only past the same 2^8 margin."""
+    k, v, tables, lens, q = _climbing(lens, bs, hq, hkv, q_len, seed=sum(lens) + 11 * q_len)
+    k16, v16 = k.astype(np.float16), v.astype(np.float16)
+    _assert_climbs(k16, tables, lens, q, bs, hkv)
+    qd = _dev(q)
+    out = torch.full_like(qd, float("nan"))
+    pkv.paged_prefill(out, qd, _dev(k16), _dev(v16), _dev(tables, torch.int32),
+                      _dev(lens, torch.int32), SCALE)
+    torch.cuda.synchronize()
+    ref = oracle.paged_attention(q, k16, v16, tables, lens, bs, SCALE)
+    assert_attn_close(out, ref, f"prefill lens={list(lens)} G={hq // hkv} q_len={q_len}")
