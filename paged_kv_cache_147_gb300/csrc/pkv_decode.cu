@@ -84,9 +84,13 @@ constexpr float kNegInf = -__builtin_huge_valf();
 #define PKV_DECODE_MIN_CTAS 2
 #endif
 constexpr int kMinCtasMt1 = PKV_DECODE_MIN_CTAS;
-// Ring kernels: resident CTAs per SM the register budget is sized for.
+// Ring kernels: resident CTAs per SM the register budget is sized for (the transposed-tile
+// ones fit two CTAs per SM without spilling, the 16-row ones one).
 #ifndef PKV_RING_MIN_CTAS
 #define PKV_RING_MIN_CTAS 1
+#endif
+#ifndef PKV_RING_TR_MIN_CTAS
+#define PKV_RING_TR_MIN_CTAS 2
 #endif
 // How long the CTA that merges a split unit waits for the unit's other partials before it
 // falls back to announcing its own (normally they are in within microseconds).
@@ -615,7 +619,9 @@ __device__ __forceinline__ void issue_queries(const DecodeArgs& a, const CUtenso
 // announces arrivals), so the consumers never stop at a unit boundary.
 template <int NCW, int NST, int MT, bool RING, bool APPEND, bool TR, bool FP8, bool KV3D>
 __global__ void __launch_bounds__((NCW + 2) * 32,
-                                  MT != 1 ? 1 : RING ? PKV_RING_MIN_CTAS : kMinCtasMt1)
+                                  MT != 1 ? 1
+                                  : RING  ? (TR ? PKV_RING_TR_MIN_CTAS : PKV_RING_MIN_CTAS)
+                                          : kMinCtasMt1)
 decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
   using L = Smem<NCW, NST, MT, FP8>;
@@ -1748,12 +1754,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 constexpr int kNCW = PKV_DECODE_WARPS, kNST = PKV_DECODE_STAGES;
 constexpr int kNCWRing = 4, kNSTRing = 8;
 // The ring's transposed-tile kernels (up to 8 rows): their per-chunk RoPE pass is a chain of
-// dependent shared-memory and arithmetic steps, so more consumer warps hide more of it.
+// dependent shared-memory and arithmetic steps, so more consumer warps per SM hide more of
+// it: two CTAs of four consumer warps and eight stages each (eight per SM; one CTA of six
+// warps and twelve stages measured 1.7 % slower on the ring step).
 #ifndef PKV_RING_TR_WARPS
-#define PKV_RING_TR_WARPS 6
+#define PKV_RING_TR_WARPS 4
 #endif
 #ifndef PKV_RING_TR_STAGES
-#define PKV_RING_TR_STAGES 12
+#define PKV_RING_TR_STAGES 8
 #endif
 constexpr int kNCWRingTR = PKV_RING_TR_WARPS, kNSTRingTR = PKV_RING_TR_STAGES;
 // The E4M3 cache: 8 KB stages of two chunks each (the producer's per-stage work, and the
